@@ -1,0 +1,558 @@
+"""Benchmark of the 8-bit block-wise optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one optimizer update (one call of the library's step entry point)
+over the workload's synthetic parameters and gradients, which are resident in
+HBM before timing starts.  W untimed warm-up steps, then exactly K timed steps
+bracketed by a barrier and a device synchronize; the L2 cache is flushed
+(256 MiB written) before every timed step and each step is timed with CUDA
+events on the launching stream.  Rank 0 prints one JSON line.
+
+Under torchrun (N > 1) every rank runs its own full replica of the workload
+on its own GPU (blocks are independent units with no exchange step), so the
+whole-job value is the units all ranks processed over the slowest rank's
+time ("scaling": "weak").
+
+--impl reference times the CPU oracle (the single-threaded C statement of the
+method) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "Gelem/s per optimizer step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "Gelem/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+class Workload:
+    """A tensor list, its dtype, optimizer and hyperparameters, and the
+    algorithmic bytes one step must move (reads + writes of p, g, the state
+    codes / values and the per-block absmax; the 2 KB of maps are ignored)."""
+
+    def __init__(self, name, desc, optim, dtype, sizes, bits, blocksize, hp, grad, p_std=0.02):
+        self.name, self.desc, self.optim, self.dtype = name, desc, optim, dtype
+        self.sizes, self.bits, self.blocksize, self.hp = sizes, bits, blocksize, hp
+        self.grad, self.p_std = grad, p_std
+
+    @property
+    def elements(self):
+        return int(sum(self.sizes))
+
+    def nstates(self):
+        return {"adam": 2, "adamw": 2, "ademamix": 3}.get(self.optim, 1)
+
+    def algorithmic_bytes(self, live_block_frac=1.0):
+        e = 4 if self.dtype == "f32" else 2
+        ns, B = self.nstates(), self.blocksize
+        total = 0.0
+        for n, b in zip(self.sizes, self.bits):
+            nb = (n + B - 1) // B
+            if b == 8:
+                rest = n * (2 * e + 2 * ns) + nb * 8 * ns  # p r+w, codes r+w, absmax r+w
+            else:
+                rest = n * (2 * e + 8 * ns)                # p r+w, binary32 states r+w
+            total += n * e + rest * live_block_frac        # g always read
+            if self.hp.get("max_unorm", 0.0) > 0:          # pre-pass reads g, p, states
+                total += n * 2 * e + (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
+        return int(total)
+
+
+def _cfg_adam_4096(optim="adam", B=256):
+    n = 4096 * 4096
+    return Workload(
+        f"{optim}8bit_4096x4096_f32_B{B}",
+        f"{'Adam' if optim == 'adam' else 'AdamW'}8bit blockwise, one 4096x4096 float32 tensor "
+        f"(16,777,216 elements), block {B}, g ~ N(0,1e-3) with 1% N(0,1e-1) outliers, wd 1e-2",
+        optim, "f32", [n], [8], B,
+        dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2),
+        ("outliers", 1e-3, 1e-1, 0.01))
+
+
+def _cfg_gpt2xl():
+    shapes = workloads.gpt2_xl_params()
+    sizes = [n for _, n in shapes]
+    bits = [8 if n >= 4096 else 32 for n in sizes]
+    return Workload("gpt2xl_list_bf16_adam8bit_B256_maxunorm1",
+                    "GPT-2-XL-shaped list (580 tensors, 1,557,611,200 elements), bf16 p/g, "
+                    "tensors < 4096 elements at 32-bit state, Adam8bit B256, max_unorm 1.0, wd 0.1",
+                    "adam", "bf16", sizes, bits, 256,
+                    dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1,
+                         max_unorm=1.0), ("normal", 1e-3))
+
+
+WORKLOADS = {
+    "adam_4096": lambda: _cfg_adam_4096("adam", 256),
+    "adamw_4096": lambda: _cfg_adam_4096("adamw", 256),
+    "adam_4096_b2048": lambda: _cfg_adam_4096("adam", 2048),
+    "adam_small": lambda: Workload("adam8bit_65536_f32_B256", "Adam8bit, one 65,536-element "
+                                   "float32 tensor, block 256", "adam", "f32", [65536], [8], 256,
+                                   dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8),
+                                   ("normal", 1e-3)),
+    "momentum_embedding": lambda: Workload(
+        "momentum8bit_50257x1024_bf16_B256_rowsparse_skipzeros",
+        "Momentum8bit on a 50,257 x 1,024 bf16 embedding, 90% of gradient rows exactly zero, "
+        "skip_zeros", "momentum", "bf16", [50257 * 1024], [8], 256,
+        dict(lr=0.01, beta1=0.9, skip_zeros=True), ("rows", 50257, 1024, 0.1, 1e-3)),
+    "lion_64m": lambda: Workload("lion8bit_64M_bf16_B256", "Lion8bit, 67,108,864 dense bf16",
+                                 "lion", "bf16", [1 << 26], [8], 256,
+                                 dict(lr=1e-4, beta1=0.9, beta2=0.99), ("normal", 1e-3)),
+    "momentum_64m": lambda: Workload("momentum8bit_64M_bf16_B256",
+                                     "Momentum8bit, 67,108,864 dense bf16", "momentum", "bf16",
+                                     [1 << 26], [8], 256, dict(lr=0.01, beta1=0.9),
+                                     ("normal", 1e-3)),
+    "ademamix_64m": lambda: Workload("ademamix8bit_64M_f32_B256",
+                                     "AdEMAMix8bit, 67,108,864 float32, alpha 5, betas "
+                                     "(0.9, 0.999, 0.9999), t_alpha = t_beta3 = 100",
+                                     "ademamix", "f32", [1 << 26], [8], 256,
+                                     dict(lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999,
+                                          alpha=5.0, t_alpha=100, t_beta3=100, eps=1e-8),
+                                     ("normal", 1e-3)),
+    "gpt2xl": _cfg_gpt2xl,
+}
+DEFAULT_WORKLOAD = "adam_4096"
+
+
+def _device_grad(wl, n, seed, device, torch_dtype):
+    kind = wl.grad[0]
+    if kind == "outliers":
+        return workloads.torch_normal_with_outliers(n, wl.grad[1], wl.grad[2], wl.grad[3], seed,
+                                                    device, torch_dtype)
+    if kind == "rows":
+        return workloads.torch_sparse_rows(wl.grad[1], wl.grad[2], wl.grad[3], wl.grad[4], seed,
+                                           device, torch_dtype)
+    return workloads.torch_normal(n, wl.grad[1], seed, device, torch_dtype)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, uuid=None, period_ms=20):
+        self.path = tempfile.mktemp(prefix="bnb8_clocks_", suffix=".csv")
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms={period_ms}"]
+        if uuid:
+            cmd.insert(1, f"--id={uuid}")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append(dict(t=ts, sm=float(parts[1]), sm_max=float(parts[2]),
+                                     power=parts[3], hw=parts[5], hw_thermal=parts[6],
+                                     sw_thermal=parts[7], sw_power=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        return rows
+
+
+def summarize_clocks(rows, t0, t1):
+    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05] or rows
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+            "sm_max_mhz": max(r["sm_max"] for r in inside), "reasons": sorted(reasons),
+            "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# peaks and committed ncu traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_block_wise_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name):
+    """Per-launch DRAM bytes of the step kernel from the committed ncu summary,
+    or None when it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload_name)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def build_state(bnb8, wl, device, seed=0):
+    import torch
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
+    params = []
+    for i, (n, b) in enumerate(zip(wl.sizes, wl.bits)):
+        p = workloads.torch_normal(n, wl.p_std, seed + i, device, tdt)
+        s1, s2, a1, a2 = bnb8.zero_state(p, wl.optim, b, wl.blocksize)
+        params.append(bnb8.ParamState(p, None, s1, s2, a1, a2, b))
+    return params, tdt
+
+
+def run_gpu(args, wl):
+    import torch
+    import bit_block_wise_gb300 as bnb8
+    from bit_block_wise_gb300 import build as bnb8_build
+
+    world, rank, local = setup_dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    bnb8_build.build()
+    stream = torch.cuda.current_stream()
+    q1 = bnb8.bnb8_create_qmap(wl.optim not in ("rmsprop", "adagrad")).to(device)
+    q2 = bnb8.bnb8_create_qmap(False).to(device)
+    params, tdt = build_state(bnb8, wl, device, seed=1000 * rank)
+    # a pool of gradients (fresh g every step, all resident before timing)
+    pool = 2 if wl.elements > (1 << 28) else 4
+    grads = [[_device_grad(wl, n, 7919 * (k + 1) + i + 100000 * rank, device, tdt)
+              for i, n in enumerate(wl.sizes)] for k in range(pool)]
+    hp_kw = dict(wl.hp)
+    ws_bytes = bnb8.bnb8_workspace_size(params, bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize,
+                                                             **hp_kw))
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    step_no = [0]
+
+    def one_step(k):
+        step_no[0] += 1
+        for ps, g in zip(params, grads[k % pool]):
+            ps.g = g
+        hp = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=step_no[0], **hp_kw)
+        bnb8.step(params, hp, q1, q2, workspace=workspace if ws_bytes else None, stream=stream)
+
+    for k in range(args.warmup):
+        one_step(k)
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        one_step(args.warmup + k)
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    rows = sampler.stop() if sampler else []
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(per_step), world, device)
+    ms_per_step = total_ms / args.steps
+    n_chunks8 = -(-sum(1 for b in wl.bits if b == 8) // 96)
+    n_chunks32 = -(-sum(1 for b in wl.bits if b == 32) // 96)
+    launches_per_step = n_chunks8 + n_chunks32
+    if wl.hp.get("max_unorm", 0.0) > 0:
+        launches_per_step += 1 + 2 * (n_chunks8 + n_chunks32)   # fill + pre-pass + finalize
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no, tdt)
+
+    value = world * wl.elements / (ms_per_step * 1e-3) / 1e9
+    alg_bytes = wl.algorithmic_bytes(live_frac(wl, grads[0]) if wl.hp.get("skip_zeros") else 1.0)
+    achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.desc, "name": wl.name, "elements": wl.elements,
+                   "tensors": len(wl.sizes), "blocksize": wl.blocksize, "optimizer": wl.optim,
+                   "param_dtype": wl.dtype, "state": "uint8 codes + binary32 absmax",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_step": alg_bytes,
+                     "traffic": ncu_traffic(wl.name)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": summarize_clocks(rows, t0, t1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, params, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def live_frac(wl, grads):
+    """Fraction of blocks with a nonzero gradient (skip_zeros traffic model)."""
+    import torch
+    B = wl.blocksize
+    live, total = 0, 0
+    for g in grads:
+        n = g.numel()
+        nb = n // B
+        if nb:
+            live += int((g[: nb * B].view(nb, B) != 0).any(dim=1).sum().item())
+            total += nb
+    return live / max(total, 1)
+
+
+def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no, tdt):
+    """The same step through the public API with the gradient arriving from
+    pinned host memory and the updated parameter read back every step."""
+    import torch
+    if wl.elements > (1 << 28):
+        steps = max(2, min(args.steps, 5))
+    else:
+        steps = max(3, min(args.steps, 50))
+    host_g = [torch.empty(n, dtype=tdt, pin_memory=True) for n in wl.sizes]
+    host_p = [torch.empty(n, dtype=tdt, pin_memory=True) for n in wl.sizes]
+    for hg, ps in zip(host_g, params):
+        hg.copy_(ps.g if ps.g is not None else torch.zeros_like(ps.p))
+    dev_g = [torch.empty_like(ps.p) for ps in params]
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        for dg, hg in zip(dev_g, host_g):
+            dg.copy_(hg, non_blocking=True)
+        for ps, dg in zip(params, dev_g):
+            ps.g = dg
+        step_no[0] += 1
+        hp = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=step_no[0], **wl.hp)
+        bnb8.step(params, hp, q1, q2, workspace=workspace if ws_bytes else None, stream=stream)
+        for hp_, ps in zip(host_p, params):
+            hp_.copy_(ps.p, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    esz = 4 if wl.dtype == "f32" else 2
+    return {"value": round(wl.elements / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+            "h2d_bytes_per_step": wl.elements * esz, "d2h_bytes_per_step": wl.elements * esz,
+            "ms_per_step": round(ms, 4), "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def _oracle_sample(wl, n_sample, params=None):
+    """Host copies of the first n_sample elements of the workload's first
+    tensor (device state when given, else fresh seeded values)."""
+    import oracle
+    n = min(n_sample, wl.sizes[0])
+    B = wl.blocksize
+    dt = wl.dtype
+    p = oracle.to_storage(workloads.normal(n, wl.p_std, 1), dt)
+    q1 = oracle.create_qmap(wl.optim not in ("rmsprop", "adagrad"))
+    q2 = oracle.create_qmap(False)
+    st = oracle.zero_state(wl.optim, n, 8, B, q1, q2)
+    t = oracle.TensorState(p, *st, 8)
+    if wl.grad[0] == "outliers":
+        g = workloads.normal_with_outliers(n, wl.grad[1], wl.grad[2], wl.grad[3], 2)
+    elif wl.grad[0] == "rows":
+        cols = wl.grad[2]
+        g = workloads.sparse_rows(max(1, n // cols), cols, wl.grad[3], wl.grad[4], 2)[:n]
+        if g.size < n:
+            g = np.concatenate([g, np.zeros(n - g.size, np.float32)])
+    else:
+        g = workloads.normal(n, wl.grad[1], 2)
+    return t, oracle.to_storage(g, dt), q1, q2
+
+
+def time_oracle(wl, n_sample, steps, budget_s):
+    import oracle
+    oracle.build()
+    t, g, q1, q2 = _oracle_sample(wl, n_sample)
+    hp_kw = {k: v for k, v in wl.hp.items()}
+    done = 0
+    t0 = time.perf_counter()
+    for k in range(1, steps + 1):
+        oracle.step(oracle.HParams(optim=wl.optim, step=k, **hp_kw), t, g, wl.dtype, wl.blocksize,
+                    q1, q2)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return t.p.size, done, el
+
+
+def calibrate_oracle(wl):
+    n, done, el = time_oracle(wl, 16 * wl.blocksize, 2, 10.0)
+    return el / done / n  # seconds per element
+
+
+def cpu_baseline(wl, params=None, budget_s=15.0):
+    sec_per_elem = calibrate_oracle(wl)
+    n_sample = int(max(wl.blocksize, min(wl.sizes[0], budget_s / 3 / sec_per_elem)))
+    n_sample -= n_sample % wl.blocksize or 0
+    n_sample = max(wl.blocksize, n_sample)
+    n, done, el = time_oracle(wl, n_sample, 3, budget_s)
+    value = n * done / el / 1e9
+    return {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n:,} of the workload's {wl.elements:,} elements (first tensor, "
+                      f"{n // wl.blocksize:,} blocks), {done} step(s), single-threaded C oracle, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, wl):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    total_budget = 90.0
+    sec_per_elem = calibrate_oracle(wl)
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    n_sample = int(max(wl.blocksize, min(wl.sizes[0], per_step / sec_per_elem)))
+    n_sample = max(wl.blocksize, n_sample - n_sample % wl.blocksize)
+    import oracle
+    t, g, q1, q2 = _oracle_sample(wl, n_sample)
+    for k in range(1, args.warmup + 1):
+        oracle.step(oracle.HParams(optim=wl.optim, step=k, **wl.hp), t, g, wl.dtype,
+                    wl.blocksize, q1, q2)
+    t0 = time.perf_counter()
+    for k in range(args.warmup + 1, args.warmup + args.steps + 1):
+        oracle.step(oracle.HParams(optim=wl.optim, step=k, **wl.hp), t, g, wl.dtype,
+                    wl.blocksize, q1, q2)
+    el = time.perf_counter() - t0
+    n = t.p.size
+    value = n * args.steps / el / 1e9
+    sample = (f"{n:,} of the workload's {wl.elements:,} elements per step "
+              f"({n // wl.blocksize:,} blocks of the first tensor), single-threaded C oracle")
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": wl.desc, "name": wl.name, "elements": wl.elements,
+                      "blocksize": wl.blocksize, "optimizer": wl.optim},
+           "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,309 @@
+"""Python binding of the GB300 8-bit block-wise optimizer library (libbnb8.so).
+
+Argument marshalling only: every function here packs torch tensors (device
+memory owned by the caller) into the C structures of ``include/bnb8.h`` and
+calls the entry point of the same name.  All computation runs in the CUDA
+kernels of the library; there is no CPU path.  If the library has not been
+built, or no CUDA device is present, calls raise ``RuntimeError``.
+
+The optimizer method is the 8-bit block-wise dynamic-quantized step of
+"8-bit Optimizers via Block-wise Quantization" (Dettmers et al.) with the
+optimizer set and parameters of the bitsandbytes docs page "optim_overview.md".
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbnb8.so")
+
+BNB8_OK, BNB8_EINVAL, BNB8_EUNSUPPORTED, BNB8_ECUDA, BNB8_EWORKSPACE = 0, 1, 2, 3, 4
+BNB8_F32, BNB8_BF16, BNB8_F16 = 0, 1, 2
+BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX = range(7)
+
+OPTIMS = {"adam": BNB8_ADAM, "adamw": BNB8_ADAMW, "momentum": BNB8_MOMENTUM,
+          "rmsprop": BNB8_RMSPROP, "adagrad": BNB8_ADAGRAD, "lion": BNB8_LION,
+          "ademamix": BNB8_ADEMAMIX}
+NSTATES = {"adam": 2, "adamw": 2, "momentum": 1, "rmsprop": 1, "adagrad": 1, "lion": 1,
+           "ademamix": 3}
+# bitsandbytes docs page "optim_overview.md": tensors below min_8bit_size
+# elements keep 32-bit state.
+MIN_8BIT_SIZE = 4096
+
+# every symbol include/bnb8.h declares
+EXPORTS = ("bnb8_last_error", "bnb8_version", "bnb8_create_qmap", "bnb8_quantize_blockwise",
+           "bnb8_dequantize_blockwise", "bnb8_workspace_size", "bnb8_step_2state",
+           "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm")
+
+
+class Bnb8Tensor(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("s1", ctypes.c_void_p),
+                ("s2", ctypes.c_void_p), ("absmax1", ctypes.c_void_p),
+                ("absmax2", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("state_bits", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class Bnb8Hparams(ctypes.Structure):
+    _fields_ = [("optim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("blocksize", ctypes.c_int32), ("skip_zeros", ctypes.c_int32),
+                ("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("beta3", ctypes.c_float), ("alpha", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("gnorm_scale", ctypes.c_float),
+                ("max_unorm", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("step", ctypes.c_int64), ("t_alpha", ctypes.c_int64),
+                ("t_beta3", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises RuntimeError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.bnb8_last_error.restype = ctypes.c_char_p
+        L.bnb8_last_error.argtypes = []
+        L.bnb8_version.restype = i32
+        L.bnb8_create_qmap.argtypes = [i32, vp]
+        L.bnb8_quantize_blockwise.argtypes = [vp, i32, i64, vp, i32, vp, vp, vp]
+        L.bnb8_dequantize_blockwise.argtypes = [vp, vp, vp, i32, i64, vp, i32, vp]
+        L.bnb8_workspace_size.argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
+                                          ctypes.POINTER(Bnb8Hparams)]
+        L.bnb8_workspace_size.restype = ctypes.c_size_t
+        for name in ("bnb8_step_2state", "bnb8_step_ademamix"):
+            getattr(L, name).argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
+                                         ctypes.POINTER(Bnb8Hparams), vp, vp, vp,
+                                         ctypes.c_size_t, vp]
+        L.bnb8_step_1state.argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
+                                       ctypes.POINTER(Bnb8Hparams), vp, vp, ctypes.c_size_t, vp]
+        L.bnb8_unorm.argtypes = [ctypes.POINTER(Bnb8Tensor), i32, ctypes.POINTER(Bnb8Hparams),
+                                 vp, vp, vp, vp, ctypes.c_size_t, vp]
+        for name in EXPORTS:
+            if name not in ("bnb8_last_error", "bnb8_version", "bnb8_workspace_size"):
+                getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+class Bnb8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"bnb8 status {status}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != BNB8_OK:
+        raise Bnb8Error(status, lib().bnb8_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    return {torch.float32: BNB8_F32, torch.bfloat16: BNB8_BF16, torch.float16: BNB8_F16}[t.dtype]
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---- hyperparameters -----------------------------------------------------------
+
+@dataclasses.dataclass
+class HParams:
+    """Hyperparameters of one update (defaults: docs page "optim_overview.md",
+    Optimizer2State).  ``step`` is the 1-based number of this update."""
+    optim: str = "adam"
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    beta3: float = 0.9999
+    alpha: float = 0.0
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    gnorm_scale: float = 1.0
+    max_unorm: float = 0.0
+    step: int = 1
+    t_alpha: int = 0
+    t_beta3: int = 0
+    skip_zeros: bool = False
+    blocksize: int = 256
+
+    def c(self, dtype_code: int) -> Bnb8Hparams:
+        return Bnb8Hparams(OPTIMS[self.optim], dtype_code, self.blocksize, int(bool(self.skip_zeros)),
+                           self.lr, self.beta1, self.beta2, self.beta3, self.alpha, self.eps,
+                           self.weight_decay, self.gnorm_scale, self.max_unorm, 0,
+                           int(self.step), int(self.t_alpha), int(self.t_beta3))
+
+
+@dataclasses.dataclass
+class ParamState:
+    """A parameter, its gradient and its optimizer state (torch tensors on the
+    device).  8-bit: s1/s2 uint8 codes with float32 absmax1/absmax2; 32-bit:
+    s1/s2 float32 and absmax None.  AdEMAMix: s1 = [2, n] (m1, m2),
+    absmax1 = [2, nblocks], s2 = nu."""
+    p: object
+    g: object
+    s1: object
+    s2: object = None
+    absmax1: object = None
+    absmax2: object = None
+    state_bits: int = 8
+
+    def c(self) -> Bnb8Tensor:
+        return Bnb8Tensor(_ptr(self.p), _ptr(self.g), _ptr(self.s1), _ptr(self.s2),
+                          _ptr(self.absmax1), _ptr(self.absmax2), self.p.numel(),
+                          self.state_bits, 0)
+
+
+def _tensor_array(params: Sequence[ParamState]):
+    arr = (Bnb8Tensor * max(1, len(params)))()
+    for i, ps in enumerate(params):
+        arr[i] = ps.c()
+    return arr
+
+
+# ---- entry points (same names as include/bnb8.h) -----------------------------
+
+def bnb8_version() -> int:
+    return int(lib().bnb8_version())
+
+
+def bnb8_create_qmap(is_signed: bool):
+    """The 256-level dynamic map as a float32 CPU tensor."""
+    torch = _torch()
+    out = torch.empty(256, dtype=torch.float32)
+    _check(lib().bnb8_create_qmap(int(bool(is_signed)), out.data_ptr()))
+    return out
+
+
+def bnb8_quantize_blockwise(x, qmap, blocksize: int = 256, codes=None, absmax=None, stream=None):
+    torch = _torch()
+    n = x.numel()
+    nb = (n + blocksize - 1) // blocksize
+    if codes is None:
+        codes = torch.empty(n, dtype=torch.uint8, device=x.device)
+    if absmax is None:
+        absmax = torch.empty(nb, dtype=torch.float32, device=x.device)
+    _check(lib().bnb8_quantize_blockwise(_ptr(x), _dtype_code(x), n, _ptr(qmap), blocksize,
+                                         _ptr(codes), _ptr(absmax), _stream(stream)))
+    return codes, absmax
+
+
+def bnb8_dequantize_blockwise(codes, absmax, qmap, blocksize: int = 256, out=None, dtype=None,
+                              stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(codes.numel(), dtype=dtype or torch.float32, device=codes.device)
+    _check(lib().bnb8_dequantize_blockwise(_ptr(codes), _ptr(absmax), _ptr(qmap), blocksize,
+                                           codes.numel(), _ptr(out), _dtype_code(out),
+                                           _stream(stream)))
+    return out
+
+
+def bnb8_workspace_size(params: Sequence[ParamState], hp: HParams) -> int:
+    if not params:
+        return 0
+    arr = _tensor_array(params)
+    hc = hp.c(_dtype_code(params[0].p))
+    return int(lib().bnb8_workspace_size(arr, len(params), ctypes.byref(hc)))
+
+
+def _workspace(params, hp, workspace):
+    torch = _torch()
+    need = bnb8_workspace_size(params, hp)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=params[0].p.device)
+    return workspace, workspace.numel()
+
+
+def _step(entry: str, params, hp: HParams, qmap1, qmap2, workspace, stream):
+    if not params:
+        return
+    arr = _tensor_array(params)
+    hc = hp.c(_dtype_code(params[0].p))
+    ws, ws_bytes = _workspace(params, hp, workspace)
+    fn = getattr(lib(), entry)
+    if entry == "bnb8_step_1state":
+        _check(fn(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(ws), ws_bytes,
+                  _stream(stream)))
+    else:
+        _check(fn(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2), _ptr(ws),
+                  ws_bytes, _stream(stream)))
+
+
+def bnb8_step_2state(params, hp: HParams, qmap1, qmap2, workspace=None, stream=None):
+    _step("bnb8_step_2state", params, hp, qmap1, qmap2, workspace, stream)
+
+
+def bnb8_step_1state(params, hp: HParams, qmap1, workspace=None, stream=None):
+    _step("bnb8_step_1state", params, hp, qmap1, None, workspace, stream)
+
+
+def bnb8_step_ademamix(params, hp: HParams, qmap1, qmap2, workspace=None, stream=None):
+    _step("bnb8_step_ademamix", params, hp, qmap1, qmap2, workspace, stream)
+
+
+def bnb8_unorm(params, hp: HParams, qmap1, qmap2=None, out_scale=None, workspace=None,
+               stream=None):
+    torch = _torch()
+    if out_scale is None:
+        out_scale = torch.empty(len(params), dtype=torch.float32, device=params[0].p.device)
+    arr = _tensor_array(params)
+    hc = hp.c(_dtype_code(params[0].p))
+    ws, ws_bytes = _workspace(params, hp, workspace)
+    _check(lib().bnb8_unorm(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2),
+                            _ptr(out_scale), _ptr(ws), ws_bytes, _stream(stream)))
+    return out_scale
+
+
+def step(params, hp: HParams, qmap1, qmap2=None, workspace=None, stream=None):
+    """Dispatch to the entry point of hp.optim."""
+    if hp.optim in ("adam", "adamw"):
+        bnb8_step_2state(params, hp, qmap1, qmap2, workspace, stream)
+    elif hp.optim == "ademamix":
+        bnb8_step_ademamix(params, hp, qmap1, qmap2, workspace, stream)
+    else:
+        bnb8_step_1state(params, hp, qmap1, workspace, stream)
+
+
+def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256):
+    """Allocate the all-zero optimizer state of parameter p (codes of 0.0 in
+    the signed / unsigned maps of bnb8_create_qmap, absmax 0)."""
+    torch = _torch()
+    n, dev = p.numel(), p.device
+    k = NSTATES[optim]
+    if state_bits == 32:
+        s1 = torch.zeros(n * (2 if optim == "ademamix" else 1), dtype=torch.float32, device=dev)
+        s2 = torch.zeros(n, dtype=torch.float32, device=dev) if k >= 2 else None
+        return s1, s2, None, None
+    nb = (n + blocksize - 1) // blocksize
+    signed1 = optim not in ("rmsprop", "adagrad")
+    s1 = torch.full((n * (2 if optim == "ademamix" else 1),), 127 if signed1 else 0,
+                    dtype=torch.uint8, device=dev)
+    a1 = torch.zeros(nb * (2 if optim == "ademamix" else 1), dtype=torch.float32, device=dev)
+    s2 = a2 = None
+    if k >= 2:
+        s2 = torch.zeros(n, dtype=torch.uint8, device=dev)
+        a2 = torch.zeros(nb, dtype=torch.float32, device=dev)
+    return s1, s2, a1, a2

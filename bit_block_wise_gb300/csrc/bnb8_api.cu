@@ -1,0 +1,540 @@
+// bnb8_api.cu -- the C ABI of include/bnb8.h: argument validation, per-step
+// scalars (binary64, rounded once), tensor lists split into 8-bit and 32-bit
+// launches, workspace layout, and the kernel launches.  Host code is built
+// with -ffp-contract=off so every scalar below is one fixed expression.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "bnb8.h"
+#include "bnb8_internal.h"
+
+using namespace bnb8;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(BNB8_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size(int dtype) { return dtype == BNB8_F32 ? 4 : 2; }
+
+bool valid_dtype(int dtype) { return dtype == BNB8_F32 || dtype == BNB8_BF16 || dtype == BNB8_F16; }
+
+int log2_blocksize(int blocksize) {
+  for (int l = 6; l <= 12; ++l)
+    if (blocksize == (1 << l)) return l;
+  return -1;
+}
+
+int nstates(int optim) {
+  if (optim == BNB8_ADAM || optim == BNB8_ADAMW) return 2;
+  if (optim == BNB8_ADEMAMIX) return 3;
+  return 1;
+}
+
+int nmaps(int optim) {
+  return (optim == BNB8_ADAM || optim == BNB8_ADAMW || optim == BNB8_ADEMAMIX) ? 2 : 1;
+}
+
+// SM count of the current device (cached per device).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+// ---- per-step scalars -------------------------------------------------------
+// Adam / AdamW: lr/(1-b1^t) * m/(sqrt(v)/sqrt(1-b2^t) + eps) is evaluated as
+// step_size * m/(sqrt(v) + eps_hat) with step_size = lr*sqrt(bc2)/bc1 and
+// eps_hat = eps*sqrt(bc2).  AdEMAMix (alpha and beta3 warm-up of the AdEMAMix
+// optimizer, t_alpha / t_beta3 on the docs page): alpha_t = min(t*alpha/T_a,
+// alpha), beta3_t = min(exp(ln b1 ln b3 / ((1 - t/T_b) ln b3 + (t/T_b) ln b1)), b3).
+struct Scalars {
+  float b1, b2, b3t, omb1, omb2, omb3t, step_size, eps_hat, inv_bc1, alpha_t, decay;
+  double unorm_c;
+};
+
+Scalars make_scalars(const bnb8_hparams& hp) {
+  Scalars s;
+  std::memset(&s, 0, sizeof(s));
+  const double t = static_cast<double>(hp.step);
+  const double b1 = hp.beta1, b2 = hp.beta2, b3 = hp.beta3;
+  const double lr = hp.lr, eps = hp.eps, wd = hp.weight_decay;
+  const double bc1 = 1.0 - std::pow(b1, t);
+  const double bc2 = 1.0 - std::pow(b2, t);
+  s.b1 = hp.beta1;
+  s.b2 = hp.beta2;
+  s.omb1 = static_cast<float>(1.0 - b1);
+  s.omb2 = static_cast<float>(1.0 - b2);
+  s.decay = static_cast<float>(1.0 - lr * wd);
+  s.step_size = hp.lr;
+  s.eps_hat = hp.eps;
+  s.unorm_c = 1.0;
+  if (hp.optim == BNB8_ADAM || hp.optim == BNB8_ADAMW) {
+    s.step_size = static_cast<float>(lr * std::sqrt(bc2) / bc1);
+    s.eps_hat = static_cast<float>(eps * std::sqrt(bc2));
+    s.unorm_c = std::sqrt(bc2) / bc1;
+  } else if (hp.optim == BNB8_ADEMAMIX) {
+    const double alpha = hp.alpha;
+    double at = alpha;
+    if (hp.t_alpha > 0) {
+      const double ramp = t * alpha / static_cast<double>(hp.t_alpha);
+      at = ramp < alpha ? ramp : alpha;
+    }
+    double b3t = b3;
+    if (hp.t_beta3 > 0) {
+      const double r = t / static_cast<double>(hp.t_beta3);
+      const double lb1 = std::log(b1), lb3 = std::log(b3);
+      const double v = std::exp(lb1 * lb3 / ((1.0 - r) * lb3 + r * lb1));
+      b3t = v < b3 ? v : b3;
+    }
+    s.alpha_t = static_cast<float>(at);
+    s.b3t = static_cast<float>(b3t);
+    s.omb3t = static_cast<float>(1.0 - static_cast<double>(s.b3t));
+    s.inv_bc1 = static_cast<float>(1.0 / bc1);
+    s.step_size = static_cast<float>(lr * std::sqrt(bc2));
+    s.eps_hat = static_cast<float>(eps * std::sqrt(bc2));
+    s.unorm_c = std::sqrt(bc2);
+  }
+  return s;
+}
+
+int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int* log2B) {
+  if (hp == nullptr) return fail(BNB8_EINVAL, "hparams is NULL");
+  bool ok = false;
+  for (int i = 0; i < nallowed; ++i) ok = ok || hp->optim == allowed[i];
+  if (!ok) return fail(BNB8_EINVAL, "optimizer %d not handled by this entry point", hp->optim);
+  if (!valid_dtype(hp->dtype)) return fail(BNB8_EINVAL, "unknown dtype %d", hp->dtype);
+  *log2B = log2_blocksize(hp->blocksize);
+  if (*log2B < 0) return fail(BNB8_EINVAL, "blocksize %d is not a power of two in [64, 4096]", hp->blocksize);
+  if (hp->reserved != 0) return fail(BNB8_EINVAL, "hparams.reserved must be 0");
+  if (hp->step < 1) return fail(BNB8_EINVAL, "step must be >= 1 (got %lld)", (long long)hp->step);
+  if (hp->t_alpha < 0 || hp->t_beta3 < 0) return fail(BNB8_EINVAL, "t_alpha / t_beta3 must be >= 0");
+  if (!(hp->max_unorm >= 0.0f) || std::isinf(hp->max_unorm))
+    return fail(BNB8_EINVAL, "max_unorm must be finite and >= 0");
+  return BNB8_OK;
+}
+
+// Validate one descriptor; sets *vec to whether every stream is aligned for
+// the vector path.
+int check_tensor(const bnb8_tensor& t, int i, const bnb8_hparams& hp, bool* vec) {
+  if (t.n < 0) return fail(BNB8_EINVAL, "tensor %d: n < 0", i);
+  if (t.reserved != 0) return fail(BNB8_EINVAL, "tensor %d: reserved must be 0", i);
+  if (t.state_bits != 8 && t.state_bits != 32)
+    return fail(BNB8_EINVAL, "tensor %d: state_bits must be 8 or 32 (got %d)", i, t.state_bits);
+  if (t.n > (int64_t(1) << 50)) return fail(BNB8_EINVAL, "tensor %d: n too large", i);
+  *vec = false;
+  if (t.n == 0) return BNB8_OK;
+  const int ns = nstates(hp.optim);
+  const int es = elem_size(hp.dtype);
+  if (t.p == nullptr || t.g == nullptr || t.s1 == nullptr)
+    return fail(BNB8_EINVAL, "tensor %d: p, g and s1 must not be NULL", i);
+  if (ns >= 2 && t.s2 == nullptr) return fail(BNB8_EINVAL, "tensor %d: s2 must not be NULL", i);
+  if (!aligned(t.p, es) || !aligned(t.g, es))
+    return fail(BNB8_EINVAL, "tensor %d: p and g must be aligned to their element size", i);
+  if (t.state_bits == 8) {
+    if (t.absmax1 == nullptr || (ns >= 2 && nmaps(hp.optim) == 2 && t.absmax2 == nullptr))
+      return fail(BNB8_EINVAL, "tensor %d: absmax arrays must not be NULL for 8-bit state", i);
+    if (!aligned(t.absmax1, 4) || (t.absmax2 != nullptr && !aligned(t.absmax2, 4)))
+      return fail(BNB8_EINVAL, "tensor %d: absmax arrays must be 4-byte aligned", i);
+  } else {
+    if (!aligned(t.s1, 4) || (t.s2 != nullptr && !aligned(t.s2, 4)))
+      return fail(BNB8_EINVAL, "tensor %d: 32-bit states must be 4-byte aligned", i);
+  }
+  bool v = aligned(t.p, 16) && aligned(t.g, 16);
+  if (t.state_bits == 8) {
+    v = v && aligned(t.s1, 8) && (ns < 2 || aligned(t.s2, 8));
+    if (hp.optim == BNB8_ADEMAMIX) v = v && (t.n % 8 == 0);
+  } else {
+    v = v && aligned(t.s1, 16) && (ns < 2 || aligned(t.s2, 16));
+    if (hp.optim == BNB8_ADEMAMIX) v = v && (t.n % 4 == 0);
+  }
+  *vec = v;
+  return BNB8_OK;
+}
+
+struct Plan {
+  struct Chunk {
+    int bits;
+    std::vector<int> idx;          // positions in the caller's list
+    int64_t total_blocks = 0;
+    int64_t partial_offset = 0;    // first block in the workspace partials
+  };
+  std::vector<Chunk> chunks;
+  std::vector<char> vec;
+  int64_t all_blocks = 0;
+};
+
+int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
+              const float* qmap1, const float* qmap2, Plan* plan) {
+  if (nt < 0) return fail(BNB8_EINVAL, "ntensors < 0");
+  if (nt > 0 && ts == nullptr) return fail(BNB8_EINVAL, "tensors is NULL");
+  plan->vec.assign(nt, 0);
+  bool any8 = false;
+  for (int i = 0; i < nt; ++i) {
+    bool v = false;
+    const int rc = check_tensor(ts[i], i, hp, &v);
+    if (rc != BNB8_OK) return rc;
+    plan->vec[i] = v ? 1 : 0;
+    if (ts[i].n > 0 && ts[i].state_bits == 8) any8 = true;
+  }
+  if (any8) {
+    if (qmap1 == nullptr || (nmaps(hp.optim) == 2 && qmap2 == nullptr))
+      return fail(BNB8_EINVAL, "8-bit tensors need qmap1%s", nmaps(hp.optim) == 2 ? " and qmap2" : "");
+    if (!aligned(qmap1, 4) || (qmap2 != nullptr && !aligned(qmap2, 4)))
+      return fail(BNB8_EINVAL, "qmaps must be 4-byte aligned");
+  }
+  int64_t offset = 0;
+  for (int bits : {8, 32}) {
+    Plan::Chunk cur;
+    cur.bits = bits;
+    for (int i = 0; i < nt; ++i) {
+      if (ts[i].n == 0 || ts[i].state_bits != bits) continue;
+      if (static_cast<int>(cur.idx.size()) == kMaxTensors) {
+        cur.partial_offset = offset;
+        offset += cur.total_blocks;
+        plan->chunks.push_back(cur);
+        cur = Plan::Chunk();
+        cur.bits = bits;
+      }
+      cur.idx.push_back(i);
+      cur.total_blocks += (ts[i].n + (int64_t(1) << log2B) - 1) >> log2B;
+    }
+    if (!cur.idx.empty()) {
+      cur.partial_offset = offset;
+      offset += cur.total_blocks;
+      plan->chunks.push_back(cur);
+    }
+  }
+  plan->all_blocks = offset;
+  return BNB8_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes_for(int nt, int64_t all_blocks) {
+  return align256(static_cast<size_t>(nt) * sizeof(float)) +
+         align256(static_cast<size_t>(all_blocks) * sizeof(float2));
+}
+
+StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan,
+                   const bnb8_hparams& hp, const Scalars& sc, int log2B, const float* qmap1,
+                   const float* qmap2) {
+  StepArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.b1 = sc.b1;
+  a.b2 = sc.b2;
+  a.b3t = sc.b3t;
+  a.omb1 = sc.omb1;
+  a.omb2 = sc.omb2;
+  a.omb3t = sc.omb3t;
+  a.step_size = sc.step_size;
+  a.eps_hat = sc.eps_hat;
+  a.inv_bc1 = sc.inv_bc1;
+  a.alpha_t = sc.alpha_t;
+  a.decay = sc.decay;
+  a.wd = hp.weight_decay;
+  a.gscale = hp.gnorm_scale;
+  a.skip_zeros = hp.skip_zeros != 0;
+  a.log2B = log2B;
+  a.ntensors = static_cast<int32_t>(c.idx.size());
+  a.total_blocks = c.total_blocks;
+  a.qmap1 = qmap1;
+  a.qmap2 = qmap2;
+  int64_t fb = 0;
+  for (size_t k = 0; k < c.idx.size(); ++k) {
+    const bnb8_tensor& t = ts[c.idx[k]];
+    DevTensor& d = a.t[k];
+    d.p = t.p;
+    d.g = t.g;
+    d.s1 = t.s1;
+    d.s2 = t.s2;
+    d.a1 = t.absmax1;
+    d.a2 = t.absmax2;
+    d.n = t.n;
+    d.first_block = fb;
+    d.index = c.idx[k];
+    d.vec_ok = plan.vec[c.idx[k]];
+    fb += (t.n + (int64_t(1) << log2B) - 1) >> log2B;
+  }
+  return a;
+}
+
+cudaError_t launch_family(int bits, int optim, int dtype, int mode, const StepArgs& a, int grid,
+                          cudaStream_t s) {
+  if (optim == BNB8_ADAM || optim == BNB8_ADAMW) return launch_step_adam(bits, optim, dtype, mode, a, grid, s);
+  if (optim == BNB8_ADEMAMIX) return launch_step_ademamix(bits, optim, dtype, mode, a, grid, s);
+  return launch_step_1state(bits, optim, dtype, mode, a, grid, s);
+}
+
+int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int log2B) {
+  static int cache[2][7][3][2] = {};
+  int& c = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
+  if (c == 0) {
+    if (optim == BNB8_ADAM || optim == BNB8_ADAMW) c = ctas_step_adam(bits, optim, dtype, mode);
+    else if (optim == BNB8_ADEMAMIX) c = ctas_step_ademamix(bits, optim, dtype, mode);
+    else c = ctas_step_1state(bits, optim, dtype, mode);
+  }
+  const int groups_per_cta = kThreads / ((1 << log2B) >> 3);
+  const int64_t need = (total_blocks + groups_per_cta - 1) / groups_per_cta;
+  const int64_t persistent = static_cast<int64_t>(sm_count()) * c;
+  return static_cast<int>(need < persistent ? need : persistent);
+}
+
+// max_unorm pre-pass + finalize into out_scale[caller index].
+int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparams& hp,
+              const Scalars& sc, int log2B, const float* qmap1, const float* qmap2,
+              float* out_scale, float2* partials, cudaStream_t stream) {
+  cudaError_t e = launch_fill(out_scale, nt, 1.0f, stream);  // n == 0 tensors keep 1
+  if (e != cudaSuccess) return cuda_fail(e, "unorm fill");
+  for (const Plan::Chunk& c : plan.chunks) {
+    StepArgs a = make_args(c, ts, plan, hp, sc, log2B, qmap1, qmap2);
+    a.partials = partials + c.partial_offset;
+    const int grid = grid_for(c.bits, hp.optim, hp.dtype, MODE_NORM, c.total_blocks, log2B);
+    e = launch_family(c.bits, hp.optim, hp.dtype, MODE_NORM, a, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "unorm pre-pass launch");
+    FinalizeArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.partials = a.partials;
+    f.out_scale = out_scale;
+    f.unorm_c = sc.unorm_c;
+    f.max_unorm = hp.max_unorm;
+    f.ntensors = a.ntensors;
+    for (int k = 0; k < a.ntensors; ++k) {
+      f.first_block[k] = a.t[k].first_block;
+      f.index[k] = a.t[k].index;
+    }
+    f.first_block[a.ntensors] = c.total_blocks;
+    e = launch_unorm_finalize(f, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "unorm finalize launch");
+  }
+  (void)nt;
+  return BNB8_OK;
+}
+
+int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int* allowed,
+                int nallowed, const float* qmap1, const float* qmap2, void* ws, size_t ws_bytes,
+                cudaStream_t stream) {
+  int log2B = 0;
+  int rc = check_hparams(hp, allowed, nallowed, &log2B);
+  if (rc != BNB8_OK) return rc;
+  Plan plan;
+  rc = make_plan(ts, nt, *hp, log2B, qmap1, qmap2, &plan);
+  if (rc != BNB8_OK) return rc;
+  if (plan.chunks.empty()) return BNB8_OK;
+  const Scalars sc = make_scalars(*hp);
+  const float* clip = nullptr;
+  if (hp->max_unorm > 0.0f) {
+    const size_t need = workspace_bytes_for(nt, plan.all_blocks);
+    if (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)
+      return fail(BNB8_EWORKSPACE, "max_unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+                  need, ws_bytes);
+    float* scales = static_cast<float*>(ws);
+    float2* partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(nt * sizeof(float)));
+    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream);
+    if (rc != BNB8_OK) return rc;
+    clip = scales;
+  }
+  for (const Plan::Chunk& c : plan.chunks) {
+    StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
+    a.clip = clip;
+    const int grid = grid_for(c.bits, hp->optim, hp->dtype, MODE_STEP, c.total_blocks, log2B);
+    const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, MODE_STEP, a, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "step launch");
+  }
+  return BNB8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bnb8_last_error(void) { return g_last_error.c_str(); }
+
+int bnb8_version(void) { return 100; }
+
+// Dynamic map (see include/bnb8.h).  Levels are emitted directly in ascending
+// order: the negative levels from the largest magnitude down, zero, the
+// positive levels from the smallest up, then +1.0.
+int bnb8_create_qmap(int is_signed, float* out) {
+  if (out == nullptr) return fail(BNB8_EINVAL, "out is NULL");
+  static const double kPow10[7] = {1.0, 10.0, 100.0, 1000.0, 10000.0, 100000.0, 1000000.0};
+  auto level = [](int k, int f, int nfrac) {
+    return (0.1 + (static_cast<double>(f) + 0.5) * (0.9 / nfrac)) / kPow10[k];
+  };
+  int i = 0;
+  if (is_signed) {
+    for (int k = 0; k <= 6; ++k) {
+      const int nfrac = 1 << (6 - k);
+      for (int f = nfrac - 1; f >= 0; --f) out[i++] = static_cast<float>(-level(k, f, nfrac));
+    }
+    out[i++] = 0.0f;
+    for (int k = 6; k >= 0; --k) {
+      const int nfrac = 1 << (6 - k);
+      for (int f = 0; f < nfrac; ++f) out[i++] = static_cast<float>(level(k, f, nfrac));
+    }
+  } else {
+    out[i++] = 0.0f;
+    for (int k = 6; k >= 0; --k) {
+      const int nfrac = 1 << (7 - k);
+      for (int f = 0; f < nfrac; ++f) out[i++] = static_cast<float>(level(k, f, nfrac));
+    }
+  }
+  out[i++] = 1.0f;
+  return i == 256 ? BNB8_OK : fail(BNB8_EUNSUPPORTED, "internal: map has %d levels", i);
+}
+
+int bnb8_quantize_blockwise(const void* x, int dtype, int64_t n, const float* qmap, int blocksize,
+                            uint8_t* codes, float* absmax, struct CUstream_st* stream) {
+  if (!valid_dtype(dtype)) return fail(BNB8_EINVAL, "unknown dtype %d", dtype);
+  const int log2B = log2_blocksize(blocksize);
+  if (log2B < 0) return fail(BNB8_EINVAL, "blocksize %d is not a power of two in [64, 4096]", blocksize);
+  if (n < 0) return fail(BNB8_EINVAL, "n < 0");
+  if (n == 0) return BNB8_OK;
+  if (x == nullptr || qmap == nullptr || codes == nullptr || absmax == nullptr)
+    return fail(BNB8_EINVAL, "x, qmap, codes and absmax must not be NULL");
+  if (!aligned(x, elem_size(dtype)) || !aligned(absmax, 4) || !aligned(qmap, 4))
+    return fail(BNB8_EINVAL, "x, qmap or absmax misaligned");
+  QuantArgs a;
+  a.x = x;
+  a.codes = codes;
+  a.absmax = absmax;
+  a.qmap = qmap;
+  a.n = n;
+  a.total_blocks = (n + blocksize - 1) >> log2B;
+  a.log2B = log2B;
+  const int groups_per_cta = kThreads / (blocksize >> 3);
+  const int64_t need = (a.total_blocks + groups_per_cta - 1) / groups_per_cta;
+  const int64_t persistent = static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(dtype);
+  const int grid = static_cast<int>(need < persistent ? need : persistent);
+  const cudaError_t e = launch_quantize(dtype, a, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BNB8_OK : cuda_fail(e, "quantize launch");
+}
+
+int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const float* qmap,
+                              int blocksize, int64_t n, void* out, int dtype,
+                              struct CUstream_st* stream) {
+  if (!valid_dtype(dtype)) return fail(BNB8_EINVAL, "unknown dtype %d", dtype);
+  const int log2B = log2_blocksize(blocksize);
+  if (log2B < 0) return fail(BNB8_EINVAL, "blocksize %d is not a power of two in [64, 4096]", blocksize);
+  if (n < 0) return fail(BNB8_EINVAL, "n < 0");
+  if (n == 0) return BNB8_OK;
+  if (codes == nullptr || absmax == nullptr || qmap == nullptr || out == nullptr)
+    return fail(BNB8_EINVAL, "codes, absmax, qmap and out must not be NULL");
+  if (!aligned(out, elem_size(dtype)) || !aligned(absmax, 4) || !aligned(qmap, 4))
+    return fail(BNB8_EINVAL, "out, qmap or absmax misaligned");
+  DequantArgs a;
+  a.codes = codes;
+  a.absmax = absmax;
+  a.qmap = qmap;
+  a.out = out;
+  a.n = n;
+  a.log2B = log2B;
+  const int64_t chunks = (n + 7) >> 3;
+  const int64_t need = (chunks + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  const cudaError_t e = launch_dequantize(dtype, a, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BNB8_OK : cuda_fail(e, "dequantize launch");
+}
+
+size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp) {
+  static const int all[] = {BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP,
+                            BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX};
+  int log2B = 0;
+  if (check_hparams(hp, all, 7, &log2B) != BNB8_OK) return 0;
+  if (hp->max_unorm <= 0.0f) return 0;
+  if (ntensors < 0 || (ntensors > 0 && tensors == nullptr)) {
+    fail(BNB8_EINVAL, "bad tensor list");
+    return 0;
+  }
+  int64_t blocks = 0;
+  for (int i = 0; i < ntensors; ++i) {
+    if (tensors[i].n < 0) {
+      fail(BNB8_EINVAL, "tensor %d: n < 0", i);
+      return 0;
+    }
+    blocks += (tensors[i].n + (int64_t(1) << log2B) - 1) >> log2B;
+  }
+  return workspace_bytes_for(ntensors, blocks);
+}
+
+int bnb8_step_2state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                     const float* qmap1, const float* qmap2, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream) {
+  static const int allowed[] = {BNB8_ADAM, BNB8_ADAMW};
+  return step_common(tensors, ntensors, hp, allowed, 2, qmap1, qmap2, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bnb8_step_1state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                     const float* qmap1, void* workspace, size_t workspace_bytes,
+                     struct CUstream_st* stream) {
+  static const int allowed[] = {BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION};
+  return step_common(tensors, ntensors, hp, allowed, 4, qmap1, nullptr, workspace,
+                     workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bnb8_step_ademamix(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                       const float* qmap1, const float* qmap2, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream) {
+  static const int allowed[] = {BNB8_ADEMAMIX};
+  return step_common(tensors, ntensors, hp, allowed, 1, qmap1, qmap2, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+               const float* qmap1, const float* qmap2, float* out_scale, void* workspace,
+               size_t workspace_bytes, struct CUstream_st* stream) {
+  static const int all[] = {BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP,
+                            BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX};
+  int log2B = 0;
+  int rc = check_hparams(hp, all, 7, &log2B);
+  if (rc != BNB8_OK) return rc;
+  if (ntensors > 0 && out_scale == nullptr) return fail(BNB8_EINVAL, "out_scale is NULL");
+  if (out_scale != nullptr && !aligned(out_scale, 4)) return fail(BNB8_EINVAL, "out_scale misaligned");
+  Plan plan;
+  rc = make_plan(tensors, ntensors, *hp, log2B, qmap1, qmap2, &plan);
+  if (rc != BNB8_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (hp->max_unorm <= 0.0f || plan.chunks.empty()) {
+    const cudaError_t e = launch_fill(out_scale, ntensors, 1.0f, s);
+    return e == cudaSuccess ? BNB8_OK : cuda_fail(e, "unorm fill");
+  }
+  const size_t need = workspace_bytes_for(ntensors, plan.all_blocks);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(BNB8_EWORKSPACE, "unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+                need, workspace_bytes);
+  float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                               align256(ntensors * sizeof(float)));
+  const Scalars sc = make_scalars(*hp);
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s);
+}
+
+}  // extern "C"

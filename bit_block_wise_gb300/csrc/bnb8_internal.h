@@ -1,0 +1,96 @@
+// bnb8_internal.h -- launch arguments shared by the host library (bnb8_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bnb8 {
+
+constexpr int kThreads = 512;       // threads per CTA of every step / quantize kernel
+constexpr int kMaxTensors = 96;     // descriptors per launch (kernel parameter space)
+constexpr int kTblSize = 5892;      // search-table entries per map: 2 signs x 2946 buckets
+constexpr int kTblZero = 2946;      // entry of the smallest positive bucket
+
+enum Optim { ADAM = 0, ADAMW = 1, MOMENTUM = 2, RMSPROP = 3, ADAGRAD = 4, LION = 5, ADEMAMIX = 6 };
+enum Dtype { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+enum Mode { MODE_STEP = 0, MODE_NORM = 1 };
+
+// One tensor of a launch.  Pointers are device pointers.
+struct DevTensor {
+  void* p;
+  const void* g;
+  void* s1;      // first state (AdEMAMix: m1 then m2)
+  void* s2;      // second state (Adam v, AdEMAMix nu)
+  float* a1;     // absmax of s1 (AdEMAMix: [2, nblocks])
+  float* a2;     // absmax of s2
+  int64_t n;
+  int64_t first_block;  // index of the tensor's first block in the launch
+  int32_t index;        // position in the caller's tensor list (clip / out_scale slot)
+  int32_t vec_ok;       // every stream of this tensor is aligned for vector access
+};
+
+// Per-step scalars (host: binary64, rounded once) and the tensor table.
+struct StepArgs {
+  float b1, b2, b3t, omb1, omb2, omb3t;
+  float step_size, eps_hat, inv_bc1, alpha_t, decay, wd, gscale;
+  int32_t skip_zeros;
+  int32_t log2B;
+  int32_t ntensors;
+  int64_t total_blocks;
+  const float* qmap1;
+  const float* qmap2;
+  const float* clip;     // per-tensor step multipliers (by DevTensor::index) or nullptr
+  float2* partials;      // MODE_NORM: per-block (sum u^2, sum p^2), indexed by launch block
+  DevTensor t[kMaxTensors];
+};
+
+struct QuantArgs {
+  const void* x;
+  uint8_t* codes;
+  float* absmax;
+  const float* qmap;
+  int64_t n;
+  int64_t total_blocks;
+  int32_t log2B;
+};
+
+struct DequantArgs {
+  const uint8_t* codes;
+  const float* absmax;
+  const float* qmap;
+  void* out;
+  int64_t n;
+  int32_t log2B;
+};
+
+struct FinalizeArgs {
+  const float2* partials;
+  float* out_scale;        // indexed by DevTensor::index
+  double unorm_c;          // |update direction| = unorm_c * |u|
+  double max_unorm;
+  int32_t ntensors;
+  int64_t first_block[kMaxTensors + 1];
+  int32_t index[kMaxTensors];
+};
+
+// Kernel launchers (defined in the kernel translation units).  Each returns
+// the cudaError_t of its launch.  bits = 8 (block-wise codes) or 32.
+cudaError_t launch_step_adam(int bits, int optim, int dtype, int mode, const StepArgs& a, int grid,
+                             cudaStream_t s);
+cudaError_t launch_step_1state(int bits, int optim, int dtype, int mode, const StepArgs& a,
+                               int grid, cudaStream_t s);
+cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const StepArgs& a,
+                                 int grid, cudaStream_t s);
+cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s);
+
+// Resident CTAs per SM of a step kernel (sizes the persistent grids).
+int ctas_step_adam(int bits, int optim, int dtype, int mode);
+int ctas_step_1state(int bits, int optim, int dtype, int mode);
+int ctas_step_ademamix(int bits, int optim, int dtype, int mode);
+int quantize_ctas_per_sm(int dtype);
+
+}  // namespace bnb8

@@ -1,0 +1,190 @@
+// k_quant.cu -- stand-alone block-wise quantize / dequantize, the max_unorm
+// finalize reduction and a fill kernel (sm_103a).
+//
+// Quantize ("8-bit Optimizers via Block-wise Quantization", abstract:
+// independently normalised blocks): per block of B elements, absmax = max |x|
+// and code = number of map midpoints below x * (1/absmax), through the same
+// shared-memory bucket table as the step kernels.  Dequantize
+// ("[XPU] Implemented 8bit optimizers in triton #1692", benchmark script,
+// F.dequantize_blockwise): out = qmap[code] * absmax[block].
+#include "bnb8_device.cuh"
+
+namespace bnb8 {
+
+struct QuantSmem {
+  static constexpr int kQ = 0;
+  static constexpr int kMid = kQ + 256 * 4;
+  static constexpr int kTbl = kMid + 256 * 4;
+  static constexpr int kRed = kTbl + kTblSize * 4;
+  static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) k_quantize(const __grid_constant__ QuantArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* sq = reinterpret_cast<float*>(smem + QuantSmem::kQ);
+  float* smid = reinterpret_cast<float*>(smem + QuantSmem::kMid);
+  uint32_t* stbl = reinterpret_cast<uint32_t*>(smem + QuantSmem::kTbl);
+  float* sred = reinterpret_cast<float*>(smem + QuantSmem::kRed);
+  __shared__ int s_bad, s_below;
+  __shared__ int s_scan[32];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 256; i += kThreads) sq[i] = a.qmap[i];
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = tid; i < 256; i += kThreads) smid[i] = i < 255 ? (sq[i] + sq[i + 1]) * 0.5f : 0.0f;
+  __syncthreads();
+  build_table(smid, stbl, &s_bad, &s_below, s_scan);
+  const bool fast_map = s_bad == 0;
+
+  const int log2B = a.log2B;
+  const int GT = (1 << log2B) >> 3;
+  const int groups_per_cta = kThreads / GT;
+  const int lane = tid & 31;
+  const int glocal = tid / GT;
+  const int gtid = tid & (GT - 1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_cta;
+  const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
+  const int in_warp = GT < 32 ? lane / GT : 0;
+  const bool vec = true;  // alignment of x and codes is checked by the host for the vector path
+  int parity = 0;
+  for (int64_t base = warp_g0; base < a.total_blocks; base += stride, parity ^= 1) {
+    const int64_t gb = base + in_warp;
+    const bool active = gb < a.total_blocks;
+    const int64_t e0 = (gb << log2B) + static_cast<int64_t>(gtid) * 8;
+    const int64_t left = active ? a.n - e0 : 0;
+    const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
+    float x[8];
+    load8<DT, true>(a.x, e0, valid, vec && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0, x);
+    float r[1];
+    r[0] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[0] = fmaxf(r[0], fabsf(x[j]));
+    group_reduce<1, true>(r, GT, glocal, sred, parity);
+    if (!active) continue;
+    const float amax = r[0];
+    const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
+    uint32_t e[8];
+    if (fast_map && inv <= FLT_MAX) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = encode_fast(x[j], inv, stbl + kTblZero);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = encode_search(x[j] * inv, smid);
+    }
+    const uint32_t lo = __byte_perm(__byte_perm(e[0], e[1], 0x0062u), __byte_perm(e[2], e[3], 0x0062u), 0x5410u);
+    const uint32_t hi = __byte_perm(__byte_perm(e[4], e[5], 0x0062u), __byte_perm(e[6], e[7], 0x0062u), 0x5410u);
+    store_codes(a.codes, e0, valid, (reinterpret_cast<uintptr_t>(a.codes) & 7) == 0,
+                make_uint2(lo, hi));
+    if (gtid == 0) a.absmax[gb] = amax;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) k_dequantize(const __grid_constant__ DequantArgs a) {
+  __shared__ float sq[256];
+  sq[threadIdx.x] = a.qmap[threadIdx.x];
+  __syncthreads();
+  const bool vec_out = (reinterpret_cast<uintptr_t>(a.out) & 15) == 0;
+  const bool vec_in = (reinterpret_cast<uintptr_t>(a.codes) & 7) == 0;
+  const int64_t nchunks = (a.n + 7) >> 3;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e0 = c << 3;
+    const int64_t left = a.n - e0;
+    const int valid = left >= 8 ? 8 : static_cast<int>(left);
+    const uint2 cw = load_codes(a.codes, e0, valid, vec_in);
+    const float am = a.absmax[e0 >> a.log2B];  // B >= 64: all 8 elements share a block
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = sq[code_byte(cw, j)] * am;
+    store8<DT>(a.out, e0, valid, vec_out, x);
+  }
+}
+
+// One CTA per tensor: sums the per-block partials of the max_unorm pre-pass
+// in binary64 (fixed order) and writes the step multiplier.
+__global__ void __launch_bounds__(256) k_unorm_finalize(const __grid_constant__ FinalizeArgs a) {
+  __shared__ double su[256], sp[256];
+  const int t = blockIdx.x;
+  const int64_t b0 = a.first_block[t], b1 = a.first_block[t + 1];
+  double u = 0.0, p = 0.0;
+  for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
+    const float2 v = a.partials[b];
+    u += static_cast<double>(v.x);
+    p += static_cast<double>(v.y);
+  }
+  su[threadIdx.x] = u;
+  sp[threadIdx.x] = p;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      su[threadIdx.x] += su[threadIdx.x + o];
+      sp[threadIdx.x] += sp[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double unorm = a.unorm_c * sqrt(su[0]);
+    const double limit = a.max_unorm * sqrt(sp[0]);
+    a.out_scale[a.index[t]] = (a.max_unorm > 0.0 && unorm > limit) ? static_cast<float>(limit / unorm)
+                                                                    : 1.0f;
+  }
+}
+
+__global__ void k_fill(float* out, int n, float v) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = v;
+}
+
+cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s) {
+  constexpr int bytes = QuantSmem::kBytes;
+  static unsigned configured[3] = {0u, 0u, 0u};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  const void* fn = dtype == DT_F32 ? reinterpret_cast<const void*>(k_quantize<DT_F32>)
+                   : dtype == DT_BF16 ? reinterpret_cast<const void*>(k_quantize<DT_BF16>)
+                                      : reinterpret_cast<const void*>(k_quantize<DT_F16>);
+  if (!(configured[dtype] & bit)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured[dtype] |= bit;
+  }
+  if (dtype == DT_F32) k_quantize<DT_F32><<<grid, kThreads, bytes, s>>>(a);
+  else if (dtype == DT_BF16) k_quantize<DT_BF16><<<grid, kThreads, bytes, s>>>(a);
+  else k_quantize<DT_F16><<<grid, kThreads, bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+int quantize_ctas_per_sm(int dtype) {
+  constexpr int bytes = QuantSmem::kBytes;
+  const void* fn = dtype == DT_F32 ? reinterpret_cast<const void*>(k_quantize<DT_F32>)
+                   : dtype == DT_BF16 ? reinterpret_cast<const void*>(k_quantize<DT_BF16>)
+                                      : reinterpret_cast<const void*>(k_quantize<DT_F16>);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, bytes) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s) {
+  if (dtype == DT_F32) k_dequantize<DT_F32><<<grid, 256, 0, s>>>(a);
+  else if (dtype == DT_BF16) k_dequantize<DT_BF16><<<grid, 256, 0, s>>>(a);
+  else k_dequantize<DT_F16><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s) {
+  k_unorm_finalize<<<a.ntensors, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_fill<<<(n + 255) / 256, 256, 0, s>>>(out, n, v);
+  return cudaGetLastError();
+}
+
+}  // namespace bnb8

@@ -1,0 +1,221 @@
+// k_step8.cuh -- the fused 8-bit block-wise optimizer step (and its max_unorm
+// pre-pass) for sm_103a.
+//
+// One HBM pass per step ("8-bit Optimizers via Block-wise Quantization",
+// abstract: blocks are quantized independently, in parallel): for each
+// block of B elements a group of B/8 threads (8 elements per thread) loads
+// p, g and the uint8 codes with 16/8-byte vector loads, dequantizes the codes
+// through the map in shared memory times the block absmax, applies the
+// optimizer update in binary32, writes p, reduces the new per-block absmax
+// with warp shuffles (plus a named barrier for B > 256), and requantizes
+// through the shared-memory bucket table (one lookup per value).
+//
+// Persistent grid: every CTA builds the map tables once, then its groups
+// stride over the blocks of all tensors of the launch.
+#pragma once
+
+#include "bnb8_device.cuh"
+
+namespace bnb8 {
+
+template <int OPT>
+struct StatePtrs {
+  uint8_t* c[3];
+  float* a[3];
+};
+
+template <int OPT>
+__device__ __forceinline__ StatePtrs<OPT> state_ptrs(const DevTensor& d, int64_t nblocks) {
+  StatePtrs<OPT> r;
+  r.c[0] = static_cast<uint8_t*>(d.s1);
+  r.a[0] = d.a1;
+  if (OPT == ADEMAMIX) {
+    r.c[1] = static_cast<uint8_t*>(d.s1) + d.n;
+    r.a[1] = d.a1 + nblocks;
+    r.c[2] = static_cast<uint8_t*>(d.s2);
+    r.a[2] = d.a2;
+  } else {
+    r.c[1] = static_cast<uint8_t*>(d.s2);
+    r.a[1] = d.a2;
+    r.c[2] = nullptr;
+    r.a[2] = nullptr;
+  }
+  return r;
+}
+
+// shared memory layout (bytes)
+template <int OPT, int MODE>
+struct Step8Smem {
+  static constexpr int NM = Traits<OPT>::NM;
+  static constexpr int kQ = 0;                                   // float q[NM][256]
+  static constexpr int kMid = kQ + NM * 256 * 4;                 // float mid[NM][256]
+  static constexpr int kTbl = kMid + NM * 256 * 4;               // uint32 tbl[NM][kTblSize]
+  static constexpr int kRed = kTbl + (MODE == MODE_STEP ? NM * kTblSize * 4 : 0);
+  static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
+};
+
+template <int OPT, int DT, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ StepArgs a) {
+  constexpr int NS = Traits<OPT>::NS;
+  constexpr int NM = Traits<OPT>::NM;
+  using L = Step8Smem<OPT, MODE>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* sq = reinterpret_cast<float*>(smem + L::kQ);
+  float* smid = reinterpret_cast<float*>(smem + L::kMid);
+  uint32_t* stbl = reinterpret_cast<uint32_t*>(smem + L::kTbl);
+  float* sred = reinterpret_cast<float*>(smem + L::kRed);
+  __shared__ int s_bad[2];
+  __shared__ int s_below;
+  __shared__ int s_scan[32];
+
+  const int tid = threadIdx.x;
+  // ---- stage the maps, midpoints and (step mode) the bucket tables ----
+  for (int i = tid; i < NM * 256; i += kThreads) sq[i] = i < 256 ? a.qmap1[i] : a.qmap2[i - 256];
+  if (tid < 2) s_bad[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < NM * 256; i += kThreads) {
+    const int m = i >> 8, k = i & 255;
+    smid[i] = k < 255 ? (sq[m * 256 + k] + sq[m * 256 + k + 1]) * 0.5f : 0.0f;
+  }
+  __syncthreads();
+  if (MODE == MODE_STEP) {
+#pragma unroll
+    for (int m = 0; m < NM; ++m) build_table(smid + m * 256, stbl + m * kTblSize, &s_bad[m], &s_below, s_scan);
+  }
+  bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
+
+  // ---- group geometry ----
+  const int log2B = a.log2B;
+  const int B = 1 << log2B;
+  const int GT = B >> 3;                  // threads per block
+  const int groups_per_cta = kThreads / GT;
+  const int lane = tid & 31;
+  const int glocal = tid / GT;
+  const int gtid = tid & (GT - 1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_cta;
+  // warp-uniform loop base: the first group of this warp
+  const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
+  const int in_warp = GT < 32 ? lane / GT : 0;
+  int parity = 0;
+
+  for (int64_t base = warp_g0; base < a.total_blocks; base += stride, parity ^= 1) {
+    const int64_t gb = base + in_warp;
+    const bool active = gb < a.total_blocks;
+    const int t = active ? (a.ntensors > 1 ? find_tensor(a, gb) : 0) : 0;
+    const DevTensor& d = a.t[t];
+    const int64_t blk = active ? gb - d.first_block : 0;
+    const int64_t nblocks = (d.n + B - 1) >> log2B;
+    const int64_t e0 = (blk << log2B) + static_cast<int64_t>(gtid) * 8;
+    const int64_t left = active ? d.n - e0 : 0;
+    const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
+    const bool vec = d.vec_ok != 0;
+    const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nblocks);
+
+    float p[8], g[8];
+    uint2 cw[NS];
+    float am[NS];
+    load8<DT, false>(d.p, e0, valid, vec, p);
+    load8<DT, true>(d.g, e0, valid, vec, g);
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      cw[k] = load_codes(sp.c[k], e0, valid, vec);
+      am[k] = active ? sp.a[k][blk] : 0.0f;
+    }
+    const float clip = (a.clip != nullptr && active) ? a.clip[d.index] : 1.0f;
+    const float eff = a.step_size * clip;
+
+    float s[NS][8];
+    float usq = 0.0f, psq = 0.0f;
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float st[3];
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
+      if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
+      bool skipped = true;
+      float u = 0.0f;
+      if (j < valid) u = elem_update<OPT>(a, eff, p[j], g[j], st, skipped);
+      if (!skipped) any = true;
+      if (MODE == MODE_NORM) usq = usq + u * u;
+#pragma unroll
+      for (int k = 0; k < NS; ++k) s[k][j] = j < valid ? st[k] : 0.0f;
+    }
+
+    if constexpr (MODE == MODE_NORM) {
+      float r[2] = {usq, psq};
+      group_reduce<2, false>(r, GT, glocal, sred, parity);
+      if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
+      continue;
+    }
+
+    // ---- new absmax per state (and whether anything changed) ----
+    float r[NS + 1];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      float mx = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(s[k][j]));
+      r[k] = mx;
+    }
+    r[NS] = any ? 1.0f : 0.0f;
+    group_reduce<NS + 1, true>(r, GT, glocal, sred, parity);
+    if (!active || r[NS] == 0.0f) continue;  // nothing updated: p, codes, absmax untouched
+
+    store8<DT>(d.p, e0, valid, vec, p);
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      const int m = Traits<OPT>::map_of(k);
+      const float amax = r[k];
+      const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
+      const bool fast = fast_map[m] && inv <= FLT_MAX;
+      uint32_t e[8];
+      if (fast) {
+        const uint32_t* tz = stbl + m * kTblSize + kTblZero;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = encode_fast(s[k][j], inv, tz);
+      } else {
+        const float* md = smid + m * 256;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = encode_search(s[k][j] * inv, md);
+      }
+      // byte 2 of each e[j] is the code
+      const uint32_t lo = __byte_perm(__byte_perm(e[0], e[1], 0x0062u), __byte_perm(e[2], e[3], 0x0062u), 0x5410u);
+      const uint32_t hi = __byte_perm(__byte_perm(e[4], e[5], 0x0062u), __byte_perm(e[6], e[7], 0x0062u), 0x5410u);
+      store_codes(sp.c[k], e0, valid, vec, make_uint2(lo, hi));
+      if (gtid == 0) sp.a[k][blk] = amax;
+    }
+  }
+}
+
+template <int OPT, int DT, int MODE>
+cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
+  constexpr int bytes = Step8Smem<OPT, MODE>::kBytes;
+  static unsigned configured = 0u;  // one bit per device: the attribute is per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (!(configured & bit)) {
+    e = cudaFuncSetAttribute(k_step8<OPT, DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  k_step8<OPT, DT, MODE><<<grid, kThreads, bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int OPT, int DT, int MODE>
+int ctas_step8_t() {
+  constexpr int bytes = Step8Smem<OPT, MODE>::kBytes;
+  cudaFuncSetAttribute(k_step8<OPT, DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_step8<OPT, DT, MODE>, kThreads, bytes) !=
+      cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace bnb8

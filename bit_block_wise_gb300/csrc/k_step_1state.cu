@@ -1,0 +1,75 @@
+// k_step_1state.cu -- step kernels of the 1-state optimizers (Momentum, RMSprop, Adagrad, Lion).
+#include "k_step8.cuh"
+#include "k_step32.cuh"
+
+namespace bnb8 {
+
+#define BNB8_DISPATCH(OPTV, DTV, MODEV, CALL8, CALL32) \
+  if (optim == OPTV && dtype == DTV && mode == MODEV) \
+    return bits == 8 ? CALL8<OPTV, DTV, MODEV>(a, grid, s) : CALL32<OPTV, DTV, MODEV>(a, grid, s);
+
+cudaError_t launch_step_1state(int bits, int optim, int dtype, int mode, const StepArgs& a,
+                                int grid, cudaStream_t s) {
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  return cudaErrorInvalidValue;
+}
+
+#undef BNB8_DISPATCH
+#define BNB8_DISPATCH(OPTV, DTV, MODEV, CALL8, CALL32) \
+  if (optim == OPTV && dtype == DTV && mode == MODEV) \
+    return bits == 8 ? CALL8<OPTV, DTV, MODEV>() : CALL32<OPTV, DTV, MODEV>();
+
+int ctas_step_1state(int bits, int optim, int dtype, int mode) {
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  return 1;
+}
+
+#undef BNB8_DISPATCH
+
+}  // namespace bnb8

@@ -1,0 +1,232 @@
+/*
+ * bnb8.h -- C ABI of the GB300 (sm_103a) 8-bit block-wise optimizer library.
+ *
+ * The library implements one hot path: the optimizer step with 8-bit
+ * block-wise dynamically quantized states, as described by
+ *   - "8-bit Optimizers via Block-wise Quantization" (Dettmers et al.),
+ *     abstract: block-wise quantization (independently normalised blocks of
+ *     B elements) with a dynamic, non-linear data type;
+ *   - bitsandbytes docs "optim_overview.md": Optimizer2State /
+ *     Optimizer1State parameters (lr, betas, eps, weight_decay,
+ *     min_8bit_size, max_unorm, skip_zeros, alpha, t_alpha, t_beta3);
+ *   - "[XPU] Implemented 8bit optimizers in triton #1692", benchmark script:
+ *     the per-parameter state tensors state1/qmap1/absmax1 and
+ *     state2/qmap2/absmax2, the AdEMAMix m1_m2 stacking, and
+ *     F.dequantize_blockwise(code, absmax, A, blocksize);
+ *   - "Support skip_zeros in the XPU Triton optimizer kernels #2097":
+ *     skip_zeros semantics (raw gradient tested before weight decay).
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns an int status (enum bnb8_status).  On failure
+ *     bnb8_last_error() returns a message for the calling thread.  No
+ *     exception or abort crosses this boundary.
+ *   - Device work is enqueued asynchronously on the caller's stream
+ *     (a cudaStream_t, passed as struct CUstream_st*; NULL = legacy default
+ *     stream).  No function synchronizes the device.  BNB8_ECUDA reports a
+ *     launch error; errors raised later by the device surface on the stream.
+ *   - The caller owns every buffer.  The library allocates no device or host
+ *     memory that outlives a call; scratch comes from a caller-provided
+ *     workspace (bnb8_workspace_size).
+ *   - Pointers marked "device" must be device-accessible memory of the
+ *     current device.  Calls are reentrant; calls on different streams that
+ *     touch the same buffers race, as with any CUDA kernel.
+ *   - Element counts are int64_t; a tensor with n == 0 is skipped.
+ *   - Dtypes: BNB8_F32 (IEEE binary32), BNB8_BF16 (bfloat16), BNB8_F16
+ *     (IEEE binary16).  All arithmetic is binary32; a value is rounded to its
+ *     storage dtype once, to nearest even.
+ *   - Block sizes: a power of two from 64 to 4096.  The last block of a
+ *     tensor may be partial.
+ */
+#ifndef BNB8_H
+#define BNB8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the type behind cudaStream_t */
+
+enum bnb8_status {
+  BNB8_OK = 0,
+  BNB8_EINVAL = 1,       /* bad argument: null pointer, size, dtype, block size, optimizer */
+  BNB8_EUNSUPPORTED = 2, /* valid request this build does not implement */
+  BNB8_ECUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  BNB8_EWORKSPACE = 4    /* workspace missing, misaligned or smaller than required */
+};
+
+enum bnb8_dtype { BNB8_F32 = 0, BNB8_BF16 = 1, BNB8_F16 = 2 };
+
+enum bnb8_optim {
+  BNB8_ADAM = 0,     /* 2-state; weight decay coupled into the gradient (torch.optim.Adam) */
+  BNB8_ADAMW = 1,    /* 2-state; decoupled weight decay (torch.optim.AdamW) */
+  BNB8_MOMENTUM = 2, /* 1-state; SGD with momentum beta1, no dampening */
+  BNB8_RMSPROP = 3,  /* 1-state; smoothing constant alpha = beta1 */
+  BNB8_ADAGRAD = 4,  /* 1-state */
+  BNB8_LION = 5,     /* 1-state; decoupled weight decay */
+  BNB8_ADEMAMIX = 6  /* two EMAs of g (m1, m2) and nu; decoupled weight decay */
+};
+
+/* One parameter tensor and its optimizer state (all device pointers).
+ *   p        parameter, n elements of hparams.dtype, updated in place.
+ *   g        gradient, n elements of the same dtype, read only.
+ *   s1, s2   state arrays.  state_bits == 8: uint8 codes; state_bits == 32:
+ *            binary32 values.  2-state optimizers: s1 = first moment
+ *            (qmap1), s2 = second moment (qmap2).  1-state: s1 only.
+ *            AdEMAMix: s1 holds m1 then m2 ([2, n], both on qmap1),
+ *            s2 holds nu (qmap2).  Unused slots may be NULL.
+ *   absmax1, absmax2
+ *            state_bits == 8 only: binary32 per-block scales, ceil(n/B)
+ *            entries for s2 and for 1-/2-state s1; AdEMAMix absmax1 is
+ *            [2, ceil(n/B)] (m1 scales, then m2 scales).
+ *   n        number of elements.
+ *   state_bits  8 (block-wise dynamic quantization) or 32 (binary32 states;
+ *            the docs page's min_8bit_size rule keeps tensors below 4096
+ *            elements at 32 bits -- the caller picks per tensor).
+ * Zero states: codes equal to the code of 0.0 in their map (127 for the
+ * signed map, 0 for the unsigned map of bnb8_create_qmap) with absmax 0, or
+ * binary32 zeros.
+ * Alignment: any element alignment is accepted; p/g/state arrays aligned to
+ * 16 bytes (codes: 8 bytes, AdEMAMix needs n % 8 == 0 for the m2 half) take
+ * the vectorised path. */
+typedef struct bnb8_tensor {
+  void* p;
+  const void* g;
+  void* s1;
+  void* s2;
+  float* absmax1;
+  float* absmax2;
+  int64_t n;
+  int32_t state_bits;
+  int32_t reserved; /* must be 0 */
+} bnb8_tensor;
+
+/* Hyperparameters of one update, shared by every tensor of a call.
+ *   optim       enum bnb8_optim; must match the entry point.
+ *   dtype       enum bnb8_dtype of p and g.
+ *   blocksize   B, a power of two in [64, 4096].
+ *   skip_zeros  nonzero: where the raw gradient is exactly 0 the parameter
+ *               and its states keep their values; a block whose gradient is
+ *               all zero keeps its codes and absmax bit-identical.
+ *   lr, beta1, beta2, eps, weight_decay   as on the docs page.
+ *   beta3, alpha, t_alpha, t_beta3        AdEMAMix only (t_* == 0: no
+ *               warm-up schedule).
+ *   gnorm_scale multiplies the raw gradient (1.0 = off).
+ *   max_unorm   0 = off.  Otherwise, per tensor, if ||update direction|| >
+ *               max_unorm * ||p|| the step is scaled down to that norm (a
+ *               pre-pass over g, p and the states; needs a workspace).
+ *   step        1-based number of this update (bias corrections, schedules). */
+typedef struct bnb8_hparams {
+  int32_t optim;
+  int32_t dtype;
+  int32_t blocksize;
+  int32_t skip_zeros;
+  float lr, beta1, beta2, beta3, alpha, eps, weight_decay, gnorm_scale, max_unorm;
+  int32_t reserved; /* must be 0 */
+  int64_t step;
+  int64_t t_alpha;
+  int64_t t_beta3;
+} bnb8_hparams;
+
+/* Message describing the last failure on this thread ("" if none). */
+const char* bnb8_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bnb8_version(void);
+
+/* Fill out[256] (host memory) with the dynamic quantization map, ascending.
+ * Data type ("8-bit Optimizers via Block-wise Quantization", abstract, and the
+ * citing description of dynamic exponent types): a sign bit (signed map
+ * only), k zero bits giving the exponent 10^-k, an indicator bit, then f
+ * fraction bits whose 2^f codes are the midpoints of 2^f equal steps of
+ * [0.1, 1].  Signed: k = 0..6, f = 6-k, plus 0 and +1.0.  Unsigned: k = 0..6,
+ * f = 7-k, plus 0 and +1.0.  Formed in binary64, rounded once.
+ * Returns BNB8_EINVAL if out is NULL. */
+int bnb8_create_qmap(int is_signed, float* out);
+
+/* Block-wise quantization (device): for each block of B elements of x,
+ * absmax[b] = max |x| over the block and codes[i] = the number of map
+ * midpoints (q[j] + q[j+1]) / 2 strictly below x[i] * (1 / absmax[b])
+ * (nearest level, ties to the lower one; 0 / absmax 0 for an all-zero block).
+ *   x       n elements of dtype.
+ *   qmap    256 binary32 map values, strictly ascending (device).
+ *   codes   n uint8 (device, written).   absmax  ceil(n/B) binary32 (written).
+ * Errors: BNB8_EINVAL for null pointers (n > 0), n < 0, bad dtype or B. */
+int bnb8_quantize_blockwise(const void* x, int dtype, int64_t n, const float* qmap, int blocksize,
+                            uint8_t* codes, float* absmax, struct CUstream_st* stream);
+
+/* Block-wise dequantization (device), the inverse used by
+ * F.dequantize_blockwise(code, absmax, A, blocksize): out[i] =
+ * qmap[codes[i]] * absmax[i / B], rounded once to dtype. */
+int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const float* qmap,
+                              int blocksize, int64_t n, void* out, int dtype,
+                              struct CUstream_st* stream);
+
+/* Bytes of workspace the step functions and bnb8_unorm need for this tensor
+ * list (0 when hp->max_unorm == 0 for the step functions).  Returns 0 and
+ * sets the error message on invalid arguments. */
+size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp);
+
+/* One optimizer update of every tensor in the list (host array of
+ * descriptors; the list is read during the call only).
+ * Per element, in binary32 (each operation rounded once, no FMA):
+ *   g = g_raw * gnorm_scale; if coupled decay and wd != 0: g = g + wd * p
+ *   Adam/AdamW  m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;
+ *               u = m / (sqrt(v) + eps*sqrt(1-b2^t));  step = lr*sqrt(1-b2^t)/(1-b1^t)
+ *   decoupled decay and wd != 0: p = p * (1 - lr*wd)
+ *   p = p - (step * clip) * u
+ * 8-bit states are dequantized (qmap[code] * absmax), updated, and
+ * requantized with a fresh per-block absmax after p is written from the
+ * unquantized new states.  skip_zeros and max_unorm as in bnb8_hparams.
+ *   qmap1, qmap2  device maps (256 binary32, ascending) for s1 and s2 of
+ *                 8-bit tensors; unused for 32-bit tensors.
+ *   workspace     device scratch of at least bnb8_workspace_size() bytes,
+ *                 256-byte aligned; may be NULL when that size is 0.
+ * Errors: BNB8_EINVAL (bad descriptor or hparams, hp->optim not ADAM/ADAMW),
+ * BNB8_EWORKSPACE, BNB8_ECUDA. */
+int bnb8_step_2state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                     const float* qmap1, const float* qmap2, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream);
+
+/* 1-state update (MOMENTUM, RMSPROP, ADAGRAD, LION); qmap1 is the map of s1
+ * (signed for Momentum and Lion, unsigned for RMSprop and Adagrad).
+ *   Momentum  m = b1*m + g;  u = m;                         step = lr
+ *   RMSprop   v = b1*v + (1-b1)*g*g;  u = g/(sqrt(v) + eps); step = lr
+ *   Adagrad   v = v + g*g;  u = g/(sqrt(v) + eps);           step = lr
+ *   Lion      c = b1*m + (1-b1)*g;  u = sign(c);  m = b2*m + (1-b2)*g;  step = lr
+ * Momentum, RMSprop and Adagrad couple weight decay into g; Lion decouples.
+ * Other arguments and errors as bnb8_step_2state. */
+int bnb8_step_1state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                     const float* qmap1, void* workspace, size_t workspace_bytes,
+                     struct CUstream_st* stream);
+
+/* AdEMAMix update: m1 = b1*m1 + (1-b1)*g;  m2 = b3_t*m2 + (1-b3_t)*g;
+ * nu = b2*nu + (1-b2)*g*g;
+ * u = (m1 / (1-b1^t) + alpha_t*m2) / (sqrt(nu) + eps*sqrt(1-b2^t));
+ * step = lr*sqrt(1-b2^t); decoupled decay.  alpha_t = min(t*alpha/t_alpha,
+ * alpha) and b3_t = min(exp(ln b1 ln b3 / ((1-t/T) ln b3 + (t/T) ln b1)), b3)
+ * with T = t_beta3 (no schedule when t_alpha / t_beta3 are 0).  m1 and m2
+ * share qmap1 (s1 = [2, n], absmax1 = [2, nblocks]); nu uses qmap2. */
+int bnb8_step_ademamix(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                       const float* qmap1, const float* qmap2, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream);
+
+/* The max_unorm pre-pass on its own: writes, for every tensor i of the list,
+ * out_scale[i] (device binary32) = the step multiplier the update would use
+ * (max_unorm * ||p|| / ||d|| if ||d|| > max_unorm * ||p||, else 1), where d
+ * is the update direction of this step without lr and without decoupled
+ * decay (Adam: u*sqrt(1-b2^t)/(1-b1^t); AdEMAMix: u*sqrt(1-b2^t); 1-state:
+ * u) and skipped elements contribute 0.  Nothing else is written.
+ * qmap2 may be NULL for 1-state optimizers.  Needs a workspace of
+ * bnb8_workspace_size() bytes computed with this hp (max_unorm > 0). */
+int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+               const float* qmap1, const float* qmap2, float* out_scale, void* workspace,
+               size_t workspace_bytes, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BNB8_H */

@@ -13,6 +13,7 @@ like the optimizer does.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import dataclasses
 import os
@@ -91,32 +92,63 @@ class _Scalars(ctypes.Structure):
 _lib = None
 
 
+def _configure(L):
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    L.oracle_create_qmap.argtypes = [ctypes.c_int, vp]
+    L.oracle_midpoints.argtypes = [vp, vp]
+    L.oracle_code.argtypes = [vp, ctypes.c_float]
+    L.oracle_code.restype = ctypes.c_int
+    L.oracle_quantize_blockwise.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, vp]
+    L.oracle_dequantize_blockwise.argtypes = [vp, vp, vp, i64, i64, vp, ctypes.c_int]
+    L.oracle_scalars.argtypes = [ctypes.POINTER(_HParams), ctypes.POINTER(_Scalars)]
+    L.oracle_unorm_scale.argtypes = [ctypes.POINTER(_HParams), vp, vp, vp, vp, vp, vp, i64,
+                                     ctypes.c_int, ctypes.c_int, i64, vp, vp,
+                                     ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_double)]
+    L.oracle_unorm_scale.restype = ctypes.c_float
+    L.oracle_step.argtypes = [ctypes.POINTER(_HParams), vp, vp, vp, vp, vp, vp, i64,
+                              ctypes.c_int, ctypes.c_int, i64, vp, vp]
+    L.oracle_step.restype = ctypes.c_float
+    L.oracle_step_clipped.argtypes = L.oracle_step.argtypes + [ctypes.c_float]
+    L.oracle_step_clipped.restype = ctypes.c_float
+    L.oracle_convert.argtypes = [vp, i64, vp, ctypes.c_int]
+    L.oracle_widen.argtypes = [vp, ctypes.c_int, i64, vp]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB_PATH)
-        vp, i64, f32p = ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_float)
-        L.oracle_create_qmap.argtypes = [ctypes.c_int, vp]
-        L.oracle_midpoints.argtypes = [vp, vp]
-        L.oracle_code.argtypes = [vp, ctypes.c_float]
-        L.oracle_code.restype = ctypes.c_int
-        L.oracle_quantize_blockwise.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, vp]
-        L.oracle_dequantize_blockwise.argtypes = [vp, vp, vp, i64, i64, vp, ctypes.c_int]
-        L.oracle_scalars.argtypes = [ctypes.POINTER(_HParams), ctypes.POINTER(_Scalars)]
-        L.oracle_unorm_scale.argtypes = [ctypes.POINTER(_HParams), vp, vp, vp, vp, vp, vp, i64,
-                                         ctypes.c_int, ctypes.c_int, i64, vp, vp,
-                                         ctypes.POINTER(ctypes.c_double),
-                                         ctypes.POINTER(ctypes.c_double)]
-        L.oracle_unorm_scale.restype = ctypes.c_float
-        L.oracle_step.argtypes = [ctypes.POINTER(_HParams), vp, vp, vp, vp, vp, vp, i64,
-                                  ctypes.c_int, ctypes.c_int, i64, vp, vp]
-        L.oracle_step.restype = ctypes.c_float
-        L.oracle_convert.argtypes = [vp, i64, vp, ctypes.c_int]
-        L.oracle_widen.argtypes = [vp, ctypes.c_int, i64, vp]
-        del f32p
-        _lib = L
+        _lib = _configure(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Run the oracle API against another build of the C source (the test
+    suite plants mistakes in copies of it to show that the pins catch them)."""
+    global _lib
+    saved = _lib
+    _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def compile_variant(source_text: str, out_path: str) -> str:
+    """Compile C source text with the oracle's flags into out_path."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.check_call(["gcc", *CFLAGS, "-o", out_path, src, "-lm"])
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 @dataclasses.dataclass
@@ -285,13 +317,16 @@ def unorm_scale(hp: HParams, t: TensorState, g: np.ndarray, dtype: str, blocksiz
 
 
 def step(hp: HParams, t: TensorState, g: np.ndarray, dtype: str, blocksize: int, q1=None,
-         q2=None) -> float:
-    """One optimizer update of tensor ``t`` in place; returns the clip multiplier."""
+         q2=None, clip: float | None = None) -> float:
+    """One optimizer update of tensor ``t`` in place; returns the clip multiplier.
+    ``clip`` (>= 0) supplies the max_unorm multiplier of the whole tensor when
+    ``t`` holds only some of its blocks."""
     hc = hp.c()
     if t.state_bits == 8:
         assert q1 is not None and (NSTATES[hp.optim] == 1 or q2 is not None)
         q1 = np.ascontiguousarray(q1, dtype=np.float32)
         q2 = None if q2 is None else np.ascontiguousarray(q2, dtype=np.float32)
-    return float(lib().oracle_step(ctypes.byref(hc), _ptr(t.p), _ptr(g), _ptr(t.s1), _ptr(t.s2),
-                                   _ptr(t.absmax1), _ptr(t.absmax2), t.p.size, t.state_bits,
-                                   DTYPES[dtype], blocksize, _ptr(q1), _ptr(q2)))
+    return float(lib().oracle_step_clipped(
+        ctypes.byref(hc), _ptr(t.p), _ptr(g), _ptr(t.s1), _ptr(t.s2), _ptr(t.absmax1),
+        _ptr(t.absmax2), t.p.size, t.state_bits, DTYPES[dtype], blocksize, _ptr(q1), _ptr(q2),
+        -1.0 if clip is None else float(clip)))

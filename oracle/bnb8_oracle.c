@@ -511,14 +511,19 @@ float oracle_unorm_scale(const oracle_hparams* hp, const void* p, const void* g,
  * 32-bit states ([P2] min_8bit_size: smaller tensors keep 32-bit state): the
  * same element update with binary32 state arrays.
  * Returns the step multiplier applied (1 unless max_unorm clipped).
+ * oracle_step_clipped takes the multiplier from the caller (clip_in >= 0)
+ * so that a subset of a tensor's blocks can be stepped with the multiplier
+ * of the whole tensor; blocks are otherwise independent.
  */
-float oracle_step(const oracle_hparams* hp, void* p, const void* g, void* s1, void* s2,
-                  float* absmax1, float* absmax2, int64_t n, int state_bits, int dtype, int64_t B,
-                  const float* q1, const float* q2) {
+float oracle_step_clipped(const oracle_hparams* hp, void* p, const void* g, void* s1, void* s2,
+                          float* absmax1, float* absmax2, int64_t n, int state_bits, int dtype,
+                          int64_t B, const float* q1, const float* q2, float clip_in) {
   step_scalars sc;
   oracle_scalars(hp, &sc);
   float clip = 1.0f;
-  if (hp->max_unorm > 0.0f)
+  if (clip_in >= 0.0f)
+    clip = clip_in; /* a multiplier the caller took from oracle_unorm_scale on the whole tensor */
+  else if (hp->max_unorm > 0.0f)
     clip = oracle_unorm_scale(hp, p, g, s1, s2, absmax1, absmax2, n, state_bits, dtype, B, q1,
                               q2, NULL, NULL);
   float step_eff = sc.step_size * clip;
@@ -579,4 +584,13 @@ float oracle_step(const oracle_hparams* hp, void* p, const void* g, void* s1, vo
   free(pnew);
   free(skipped);
   return clip;
+}
+
+/* The step on a whole tensor: the max_unorm multiplier (if any) is computed
+ * from this tensor. */
+float oracle_step(const oracle_hparams* hp, void* p, const void* g, void* s1, void* s2,
+                  float* absmax1, float* absmax2, int64_t n, int state_bits, int dtype, int64_t B,
+                  const float* q1, const float* q2) {
+  return oracle_step_clipped(hp, p, g, s1, s2, absmax1, absmax2, n, state_bits, dtype, B, q1, q2,
+                             -1.0f);
 }

@@ -1,0 +1,298 @@
+"""GPU parity: the CUDA library (called through its C ABI via the binding)
+against the CPU oracle, element by element, on seeded inputs.
+
+Bar: codes and absmax bit-exact; parameters bit-exact too (the kernels run
+the oracle's binary32 operation sequence with IEEE division and square root
+and no FMA contraction), except where max_unorm's norm is summed in a
+different order: there p is within 1e-6 relative (binary32) / 1 ulp (16-bit).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from parity_util import assert_same, map_pair, maps, random_state, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+S, U = maps()
+OPTIMS = ["adam", "adamw", "momentum", "rmsprop", "adagrad", "lion", "ademamix"]
+HP_BASE = {
+    "adam": dict(lr=1e-3, beta1=0.9, beta2=0.999),
+    "adamw": dict(lr=1e-3, beta1=0.9, beta2=0.999),
+    "momentum": dict(lr=0.01, beta1=0.9),
+    "rmsprop": dict(lr=0.01, beta1=0.9),
+    "adagrad": dict(lr=0.01),
+    "lion": dict(lr=1e-4, beta1=0.9, beta2=0.99),
+    "ademamix": dict(lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999, alpha=5.0, t_alpha=10,
+                     t_beta3=10),
+}
+
+
+@pytest.fixture(scope="module")
+def bnb8():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_block_wise_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def qdev(bnb8):
+    return to_dev(S), to_dev(U)
+
+
+def _host_to(x, dtype):
+    return oracle.to_storage(x, dtype)
+
+
+def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False, wd=0.0,
+             gscale=1.0, max_unorm=0.0, zero_frac=0.0, seed=0, init="random", extra_hp=None,
+             offsets=None):
+    """Run `steps` updates of a tensor list on the GPU and on the oracle and
+    compare after every step."""
+    q1, q2 = map_pair(optim, S, U)
+    qd1 = qdev[0] if q1 is S else qdev[1]
+    qd2 = None if q2 is None else qdev[1]
+    refs, params, keep = [], [], []
+    for i, n in enumerate(sizes):
+        p = _host_to(workloads.normal(n, 0.1, seed + 10 * i), dtype)
+        b = bits[i] if isinstance(bits, (list, tuple)) else bits
+        if init == "zero":
+            st = oracle.zero_state(optim, n, b, B, q1, q2)
+        else:
+            st = random_state(optim, n, b, B, seed + 10 * i + 1, q1, q2)
+        refs.append(oracle.TensorState(p.copy(), *[None if a is None else a.copy() for a in st], b))
+        dev = [to_dev(p, dtype)] + [to_dev(a) for a in st]
+        if offsets is not None and offsets[i]:
+            # misaligned storage: same values at an element offset (scalar path)
+            off = offsets[i]
+            shifted = []
+            for t in dev:
+                if t is None:
+                    shifted.append(None)
+                    continue
+                buf = torch.empty(t.numel() + off, dtype=t.dtype, device=t.device)
+                buf[off:].copy_(t)
+                keep.append(buf)
+                shifted.append(buf[off:])
+            dev = shifted
+        params.append(bnb8.ParamState(dev[0], None, dev[1], dev[2], dev[3], dev[4], b))
+    for k in range(1, steps + 1):
+        hp = dict(HP_BASE[optim])
+        hp.update(extra_hp or {})
+        hp.update(weight_decay=wd, gnorm_scale=gscale, max_unorm=max_unorm, step=k,
+                  skip_zeros=skip_zeros)
+        ghost = []
+        for i, n in enumerate(sizes):
+            g = workloads.normal(n, 1e-2, seed + 1000 * k + i)
+            if zero_frac:
+                rng = np.random.default_rng(seed + 7 * k + i)
+                g[rng.random(n) < zero_frac] = 0.0
+                # whole zero blocks too
+                nb = (n + B - 1) // B
+                for blk in rng.choice(nb, size=max(1, nb // 3), replace=False):
+                    g[blk * B:(blk + 1) * B] = 0.0
+            g = _host_to(g, dtype)
+            ghost.append(g)
+            gd = to_dev(g, dtype)
+            if offsets is not None and offsets[i]:
+                buf = torch.empty(gd.numel() + offsets[i], dtype=gd.dtype, device=gd.device)
+                buf[offsets[i]:].copy_(gd)
+                keep.append(buf)
+                gd = buf[offsets[i]:]
+            params[i].g = gd
+        bnb8.step(params, bnb8.HParams(optim=optim, blocksize=B, **hp), qd1, qd2)
+        ohp = oracle.HParams(optim=optim, **hp)
+        for i, n in enumerate(sizes):
+            oracle.step(ohp, refs[i], ghost[i], dtype, B, q1, q2)
+        torch.cuda.synchronize()
+        for i, (ps, r) in enumerate(zip(params, refs)):
+            tag = f"{optim}/{dtype}/bits{r.state_bits}/B{B}/step{k}/t{i}(n={sizes[i]})"
+            if max_unorm > 0:
+                got = oracle.to_f32(to_host(ps.p), dtype).astype(np.float64)
+                want = oracle.to_f32(r.p, dtype).astype(np.float64)
+                if dtype == "f32":
+                    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-12, err_msg=tag)
+                else:
+                    # one unit in the last place of the 16-bit format
+                    ulp = np.abs(want) * (2.0 ** -7 if dtype == "bf16" else 2.0 ** -10)
+                    assert np.all(np.abs(got - want) <= ulp + 1e-30), tag
+                # continue from identical parameters so the check stays per step
+                ps.p.copy_(to_dev(r.p, dtype))
+            else:
+                assert_same(tag + " p", to_host(ps.p), r.p)
+            assert_same(tag + " s1", to_host(ps.s1), r.s1)
+            assert_same(tag + " s2", to_host(ps.s2), r.s2)
+            assert_same(tag + " absmax1", to_host(ps.absmax1), r.absmax1)
+            assert_same(tag + " absmax2", to_host(ps.absmax2), r.absmax2)
+    return params, refs
+
+
+# ---------------------------------------------------------------------------
+# quantize / dequantize
+# ---------------------------------------------------------------------------
+
+def _special_values(n, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(n).astype(np.float32) * np.float32(0.01)
+    x[::7] = 0.0
+    x[1::11] = -0.0
+    x[2::13] = np.float32(1e-30) * rng.standard_normal(x[2::13].size).astype(np.float32)
+    x[3::17] = np.float32(3e-39)                                   # subnormal
+    x[4::19] = rng.choice(S, x[4::19].size) * np.float32(0.01)     # exact levels
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("B", [64, 128, 256, 512, 1024, 2048, 4096])
+@pytest.mark.parametrize("signed", [True, False])
+def test_quantize_matches_oracle(bnb8, dtype, B, signed):
+    q = S if signed else U
+    n = 5 * B + 77
+    x = _host_to(_special_values(n, B), dtype)
+    x_dev = to_dev(x, dtype)
+    codes, absmax = bnb8.bnb8_quantize_blockwise(x_dev, to_dev(q), B)
+    oc, oa = oracle.quantize_blockwise(x, dtype, q, B)
+    torch.cuda.synchronize()
+    assert_same("codes", to_host(codes), oc)
+    assert_same("absmax", to_host(absmax), oa)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("B", [64, 256, 4096])
+def test_dequantize_matches_oracle(bnb8, dtype, B):
+    n = 3 * B + 5
+    codes = workloads.random_codes(n, B)
+    absmax = workloads.random_absmax((n + B - 1) // B, 2.0, B + 1)
+    out = bnb8.bnb8_dequantize_blockwise(to_dev(codes), to_dev(absmax), to_dev(S), B,
+                                         dtype={"f32": torch.float32, "bf16": torch.bfloat16,
+                                                "f16": torch.float16}[dtype])
+    torch.cuda.synchronize()
+    assert_same("dequant", to_host(out), oracle.dequantize_blockwise(codes, absmax, S, B, dtype))
+
+
+def test_quantize_degenerate_blocks(bnb8):
+    # all-zero block, a block of subnormals whose reciprocal overflows, a
+    # block at the binary32 maximum, and exact map levels at power-of-two scale
+    B = 256
+    blocks = [np.zeros(B, np.float32),
+              np.full(B, np.float32(1e-45)) * np.sign(np.random.default_rng(0).standard_normal(B)).astype(np.float32),
+              np.linspace(-3.4e38, 3.4e38, B).astype(np.float32),
+              (S * np.float32(2.0 ** -20)).astype(np.float32)]
+    x = np.concatenate(blocks).astype(np.float32)
+    for q in (S, U):
+        codes, absmax = bnb8.bnb8_quantize_blockwise(to_dev(x), to_dev(q), B)
+        oc, oa = oracle.quantize_blockwise(x, "f32", q, B)
+        torch.cuda.synchronize()
+        assert_same("codes", to_host(codes), oc)
+        assert_same("absmax", to_host(absmax), oa)
+
+
+def test_quantize_fallback_map(bnb8):
+    # a map with two midpoints inside one search bucket (levels 1e-3 and
+    # 1.0001e-3) and one in the tiny bucket: the kernels must take the exact
+    # binary-search path and still match the oracle
+    q = np.sort(np.concatenate([np.linspace(-1, 1, 250), [1e-3, 1.0001e-3, 1.0002e-3, 1e-9,
+                                                          2e-9, 3e-9]]).astype(np.float32))
+    assert q.size == 256 and np.all(np.diff(q) > 0)
+    x = _special_values(4 * 256 + 9, 5)
+    x[100:140] = np.float32(1.00005e-3) * 0.01
+    codes, absmax = bnb8.bnb8_quantize_blockwise(to_dev(x), to_dev(q), 256)
+    oc, oa = oracle.quantize_blockwise(x, "f32", q, 256)
+    torch.cuda.synchronize()
+    assert_same("codes", to_host(codes), oc)
+    assert_same("absmax", to_host(absmax), oa)
+
+
+# ---------------------------------------------------------------------------
+# optimizer steps
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("bits", [8, 32])
+def test_step_matches_oracle(bnb8, qdev, optim, dtype, bits):
+    # several tiles, a ragged tail block, a single-element tensor
+    run_case(bnb8, qdev, optim, dtype, bits, 256, [7 * 256 + 77, 4096, 1], steps=3,
+             wd=1e-2, seed=1)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("B", [64, 128, 512, 2048, 4096])
+def test_step_blocksizes(bnb8, qdev, optim, B):
+    run_case(bnb8, qdev, optim, "f32", 8, B, [3 * B + 5, B], steps=2, seed=2)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_step_from_zero_state(bnb8, qdev, optim, dtype):
+    run_case(bnb8, qdev, optim, dtype, 8, 256, [5000], steps=5, init="zero", seed=3)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("bits", [8, 32])
+@pytest.mark.parametrize("B", [256, 2048])
+def test_step_skip_zeros(bnb8, qdev, optim, bits, B):
+    run_case(bnb8, qdev, optim, "bf16", bits, B, [6 * B + 3], steps=3, skip_zeros=True,
+             zero_frac=0.2, wd=1e-2, seed=4)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+def test_step_gnorm_scale_and_coupled_decay(bnb8, qdev, optim):
+    run_case(bnb8, qdev, optim, "f32", 8, 256, [3000], steps=2, wd=0.1, gscale=0.37, seed=5)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_step_max_unorm(bnb8, qdev, optim, dtype):
+    run_case(bnb8, qdev, optim, dtype, [8, 32, 8], 256, [4000, 300, 256 * 9], steps=3,
+             max_unorm=0.05, wd=1e-2, seed=6)
+
+
+@pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
+def test_unorm_scales_match_oracle(bnb8, qdev, optim):
+    q1, q2 = map_pair(optim, S, U)
+    sizes, bits = [5000, 700, 256 * 40 + 3], [8, 32, 8]
+    params, refs = [], []
+    for i, n in enumerate(sizes):
+        p = workloads.normal(n, 0.02, 70 + i)
+        st = random_state(optim, n, bits[i], 256, 80 + i, q1, q2)
+        refs.append(oracle.TensorState(p.copy(), *st, bits[i]))
+        params.append(bnb8.ParamState(to_dev(p), to_dev(workloads.normal(n, 1e-2, 90 + i)),
+                                      *[to_dev(a) for a in st], bits[i]))
+    hp = dict(HP_BASE[optim], max_unorm=0.02, step=4)
+    qd1 = qdev[0] if q1 is S else qdev[1]
+    scales = bnb8.bnb8_unorm(params, bnb8.HParams(optim=optim, **hp), qd1,
+                             None if q2 is None else qdev[1])
+    torch.cuda.synchronize()
+    got = to_host(scales)
+    for i, (ps, r) in enumerate(zip(params, refs)):
+        want, unorm, pnorm = oracle.unorm_scale(oracle.HParams(optim=optim, **hp), r,
+                                                to_host(ps.g), "f32", 256, q1, q2)
+        assert abs(got[i] - want) <= 1e-6 * want, (i, got[i], want)
+        assert got[i] < 1.0
+
+
+def test_step_multi_tensor_list_over_launch_capacity(bnb8, qdev):
+    # more tensors than one launch carries, mixed 8/32-bit, empty tensors
+    rng = np.random.default_rng(9)
+    sizes = [int(x) for x in rng.integers(1, 3000, 150)]
+    sizes[5] = 0
+    sizes[77] = 0
+    bits = [8 if n >= 1024 else 32 for n in sizes]
+    run_case(bnb8, qdev, "adam", "bf16", bits, 256, sizes, steps=2, seed=10)
+
+
+@pytest.mark.parametrize("optim", ["adam", "ademamix", "lion"])
+def test_step_unaligned_tensors(bnb8, qdev, optim):
+    # element offsets that break 16-byte alignment: the scalar path
+    run_case(bnb8, qdev, optim, "f32", 8, 256, [1000, 2049], steps=2, offsets=[1, 3], seed=11)
+    run_case(bnb8, qdev, optim, "bf16", 32, 256, [1000, 2049], steps=2, offsets=[1, 3], seed=12)
+
+
+def test_ademamix_ragged_m2_offset(bnb8, qdev):
+    # n % 8 != 0 puts the m2 codes of s1 = [2, n] off the 8-byte grid
+    run_case(bnb8, qdev, "ademamix", "f32", 8, 256, [1003, 517], steps=3, seed=13)

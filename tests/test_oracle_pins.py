@@ -70,7 +70,7 @@ def test_qmap_matches_byte_structure_enumeration(signed):
 
 def test_qmap_closed_form_values():
     gold = golden("qmap_closed_form.json")
-    for name, q in (("signed", S), ("unsigned", U)):
+    for name, q in (("signed", oracle.create_qmap(True)), ("unsigned", oracle.create_qmap(False))):
         for idx, dec in gold[name].items():
             assert q[int(idx)] == np.float32(float(dec)), (name, idx, q[int(idx)], dec)
         # number of levels in each decade [10^-(k+1), 10^-k)
@@ -82,6 +82,7 @@ def test_qmap_closed_form_values():
 
 
 def test_qmap_monotone_symmetric_endpoints():
+    S, U = oracle.create_qmap(True), oracle.create_qmap(False)
     for q in (S, U):
         assert q.dtype == np.float32 and q.shape == (256,)
         assert np.all(np.diff(q.astype(np.float64)) > 0)
@@ -96,9 +97,23 @@ def test_qmap_monotone_symmetric_endpoints():
 # storage dtypes
 # ---------------------------------------------------------------------------
 
+def _rounding_ties():
+    # binary32 values exactly halfway between two bfloat16 / binary16 values,
+    # with both parities of the last kept bit
+    rng = np.random.default_rng(7)
+    hi = rng.integers(0, 1 << 16, 4000, dtype=np.uint32)
+    bf16_ties = ((hi << 16) | 0x8000).astype(np.uint32).view(np.float32)
+    mant = rng.integers(0, 1 << 10, 4000, dtype=np.uint32)
+    expo = rng.integers(103, 143, 4000, dtype=np.uint32)            # normal binary16 range
+    f16_ties = ((expo << 23) | (mant << 13) | 0x1000).astype(np.uint32).view(np.float32)
+    sub = (rng.integers(1, 1 << 10, 2000).astype(np.float32) + np.float32(0.5)) * np.float32(2.0 ** -24)
+    return np.concatenate([bf16_ties, -bf16_ties, f16_ties, -f16_ties, sub, -sub])
+
+
 def _edge_floats():
     rng = np.random.default_rng(1)
     x = np.concatenate([
+        _rounding_ties(),
         rng.standard_normal(20000).astype(np.float32),
         (rng.standard_normal(20000) * 1e-6).astype(np.float32),
         (rng.standard_normal(5000) * 7e4).astype(np.float32),
@@ -612,6 +627,7 @@ def test_max_unorm_invariants(optim):
     assert abs(applied - np.float32(mu) * pnorm) <= 1e-3 * (mu * pnorm)
     # clipping never touches the states
     np.testing.assert_array_equal(clip.s1, plain.s1)
+    np.testing.assert_array_equal(clip.absmax1, plain.absmax1)
     # and the update direction is unchanged: dp is parallel to the unclipped step
     dp0 = plain.p.astype(np.float64) - base.p.astype(np.float64)
     cos = dp.dot(dp0) / (np.linalg.norm(dp) * np.linalg.norm(dp0))
