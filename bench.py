@@ -503,7 +503,7 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    total_budget = 90.0
+    total_budget = args.ref_budget
     sec_per_elem = calibrate_oracle(wl)
     per_step = total_budget / max(1, args.steps + args.warmup)
     n_sample = int(max(wl.blocksize, min(wl.sizes[0], per_step / sec_per_elem)))
@@ -543,7 +543,10 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the cpu_baseline leg")
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="seconds of oracle time for --impl reference (all steps)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quantize(const __grid_constant_
   const int in_warp = GT < 32 ? lane / GT : 0;
   const bool vec = true;  // alignment of x and codes is checked by the host for the vector path
   int parity = 0;
-  for (int64_t base = warp_g0; base < a.total_blocks; base += stride, parity ^= 1) {
+  for (int64_t base = warp_g0; base < a.total_blocks; base += stride) {
     const int64_t gb = base + in_warp;
     const bool active = gb < a.total_blocks;
     const int64_t e0 = (gb << log2B) + static_cast<int64_t>(gtid) * 8;
@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quantize(const __grid_constant_
 #pragma unroll
     for (int j = 0; j < 8; ++j) r[0] = fmaxf(r[0], fabsf(x[j]));
     group_reduce<1, true>(r, GT, glocal, sred, parity);
+    parity ^= 1;
     if (!active) continue;
     const float amax = r[0];
     const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
   const int in_warp = GT < 32 ? lane / GT : 0;
   int parity = 0;
 
-  for (int64_t base = warp_g0; base < a.total_blocks; base += stride, parity ^= 1) {
+  for (int64_t base = warp_g0; base < a.total_blocks; base += stride) {
     const int64_t gb = base + in_warp;
     const bool active = gb < a.total_blocks;
     const int t = active ? (a.ntensors > 1 ? find_tensor(a, gb) : 0) : 0;
@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
     if constexpr (MODE == MODE_NORM) {
       float r[2] = {usq, psq};
       group_reduce<2, false>(r, GT, glocal, sred, parity);
+      parity ^= 1;
       if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
       continue;
     }

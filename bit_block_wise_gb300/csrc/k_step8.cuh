@@ -98,7 +98,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   const int in_warp = GT < 32 ? lane / GT : 0;
   int parity = 0;
 
-  for (int64_t base = warp_g0; base < a.total_blocks; base += stride, parity ^= 1) {
+  // parity selects the half of the reduction scratch; it flips after every
+  // group reduction so that consecutive reductions never share a slot
+  for (int64_t base = warp_g0; base < a.total_blocks; base += stride) {
     const int64_t gb = base + in_warp;
     const bool active = gb < a.total_blocks;
     const int t = active ? (a.ntensors > 1 ? find_tensor(a, gb) : 0) : 0;
@@ -114,8 +116,29 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     float p[8], g[8];
     uint2 cw[NS];
     float am[NS];
-    load8<DT, false>(d.p, e0, valid, vec, p);
-    load8<DT, true>(d.g, e0, valid, vec, g);
+    if (MODE == MODE_STEP && a.skip_zeros) {
+      // skip_zeros: read g first; a block whose gradient is all zero is left
+      // untouched, so its p, codes and absmax are never read.  Groups of fewer
+      // than 32 threads skip only when their whole warp may.
+      load8<DT, true>(d.g, e0, valid, vec, g);
+      bool nz = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) nz = nz || (j < valid && g[j] != 0.0f);
+      bool group_nz;
+      if (GT <= 32) {
+        group_nz = __any_sync(0xffffffffu, nz);
+      } else {
+        float v[1] = {nz ? 1.0f : 0.0f};
+        group_reduce<1, true>(v, GT, glocal, sred, parity);
+        parity ^= 1;
+        group_nz = v[0] != 0.0f;
+      }
+      if (!group_nz) continue;
+      load8<DT, false>(d.p, e0, valid, vec, p);
+    } else {
+      load8<DT, false>(d.p, e0, valid, vec, p);
+      load8<DT, true>(d.g, e0, valid, vec, g);
+    }
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
       cw[k] = load_codes(sp.c[k], e0, valid, vec);
@@ -146,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     if constexpr (MODE == MODE_NORM) {
       float r[2] = {usq, psq};
       group_reduce<2, false>(r, GT, glocal, sred, parity);
+      parity ^= 1;
       if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
       continue;
     }
@@ -161,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     }
     r[NS] = any ? 1.0f : 0.0f;
     group_reduce<NS + 1, true>(r, GT, glocal, sred, parity);
+    parity ^= 1;
     if (!active || r[NS] == 0.0f) continue;  // nothing updated: p, codes, absmax untouched
 
     store8<DT>(d.p, e0, valid, vec, p);

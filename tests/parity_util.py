@@ -82,3 +82,30 @@ def assert_same(name, got: np.ndarray, want: np.ndarray):
         i = bad[0]
         raise AssertionError(f"{name}: {bad.size} of {got.size} differ; first at {i}: "
                              f"got {got[i]!r} want {want[i]!r}")
+
+
+def sample_blocks(n: int, B: int, count: int, seed: int):
+    """Sorted distinct block indices: the first, the last and `count` random."""
+    nb = (n + B - 1) // B
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(nb, size=min(count, nb), replace=False).tolist())
+    pick.update({0, nb - 1})
+    return sorted(pick)
+
+
+def gather(t, blocks, B: int, n: int, base: int = 0, dtype: str | None = None):
+    """Concatenate the elements of the given blocks of a device tensor (the
+    stream starting at element `base`, of logical length n) on the host."""
+    import torch
+    idx = []
+    for b in blocks:
+        lo, hi = b * B, min(n, (b + 1) * B)
+        idx.append(torch.arange(base + lo, base + hi, device=t.device))
+    sel = t[torch.cat(idx)]
+    return to_host(sel)
+
+
+def gather_absmax(a, blocks, nblocks: int, base_block: int = 0):
+    import torch
+    sel = a[torch.tensor([base_block + b for b in blocks], device=a.device)]
+    return to_host(sel)

@@ -100,6 +100,22 @@ def torch_sparse_rows(rows: int, cols: int, live_frac: float, std: float, seed: 
     return g if dtype is None else g.to(dtype)
 
 
+def torch_random_codes(n: int, seed: int, device):
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return torch.randint(0, 256, (n,), generator=gen, device=device, dtype=torch.int32).to(
+        torch.uint8)
+
+
+def torch_random_absmax(nblocks: int, scale: float, seed: int, device):
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = torch.randn(nblocks, generator=gen, device=device, dtype=torch.float32).abs_()
+    return x.mul_(scale).add_(scale * 1e-3)
+
+
 # ---- shapes ------------------------------------------------------------------
 
 
