@@ -36,7 +36,7 @@ MIN_8BIT_SIZE = 4096
 # every symbol include/bnb8.h declares
 EXPORTS = ("bnb8_last_error", "bnb8_version", "bnb8_create_qmap", "bnb8_quantize_blockwise",
            "bnb8_dequantize_blockwise", "bnb8_workspace_size", "bnb8_step_2state",
-           "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm")
+           "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm", "bnb8_unorm_static")
 
 
 class Bnb8Tensor(ctypes.Structure):
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(Bnb8Hparams), vp, vp, ctypes.c_size_t, vp]
         L.bnb8_unorm.argtypes = [ctypes.POINTER(Bnb8Tensor), i32, ctypes.POINTER(Bnb8Hparams),
                                  vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.bnb8_unorm_static.argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
+                                        ctypes.POINTER(Bnb8Hparams), vp, vp, vp, vp]
         for name in EXPORTS:
             if name not in ("bnb8_last_error", "bnb8_version", "bnb8_workspace_size"):
                 getattr(L, name).restype = i32
@@ -274,6 +276,20 @@ def bnb8_unorm(params, hp: HParams, qmap1, qmap2=None, out_scale=None, workspace
     ws, ws_bytes = _workspace(params, hp, workspace)
     _check(lib().bnb8_unorm(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2),
                             _ptr(out_scale), _ptr(ws), ws_bytes, _stream(stream)))
+    return out_scale
+
+
+def bnb8_unorm_static(params, hp: HParams, qmap1, qmap2=None, out_scale=None, stream=None):
+    """bnb8_unorm without a workspace: for callers that cannot allocate device
+    memory (the library's fixed 2 MiB scratch array holds the partial norms;
+    at most 262,144 blocks per call; calls that overlap on the GPU race)."""
+    torch = _torch()
+    if out_scale is None:
+        out_scale = torch.empty(len(params), dtype=torch.float32, device=params[0].p.device)
+    arr = _tensor_array(params)
+    hc = hp.c(_dtype_code(params[0].p))
+    _check(lib().bnb8_unorm_static(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2),
+                                   _ptr(out_scale), _stream(stream)))
     return out_scale
 
 

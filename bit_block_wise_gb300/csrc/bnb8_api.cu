@@ -538,3 +538,68 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// bnb8_unorm_static: bnb8_unorm for callers that cannot allocate device
+// memory.  The per-block partial norms live in one file-scope device array
+// instead of a caller workspace.  Every GPU that loads this library holds the
+// array (2 MiB) until the process exits; all calls on a device share it.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kStaticScratchBlocks = int64_t(1) << 18;  // float2 partials: 2 MiB
+
+__device__ __align__(256) float2 g_static_scratch[kStaticScratchBlocks];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (with that device current) and cached.  Host code must not use the
+// array's name as a pointer: on the host it only stands in for the symbol.
+int static_scratch(float2** out) {
+  static float2* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(BNB8_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  if (addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    addr[dev] = static_cast<float2*>(ptr);
+  }
+  *out = addr[dev];
+  return BNB8_OK;
+}
+
+}  // namespace
+
+extern "C" int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                                 const float* qmap1, const float* qmap2, float* out_scale,
+                                 struct CUstream_st* stream) {
+  static const int all[] = {BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP,
+                            BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX};
+  int log2B = 0;
+  int rc = check_hparams(hp, all, 7, &log2B);
+  if (rc != BNB8_OK) return rc;
+  if (ntensors > 0 && out_scale == nullptr) return fail(BNB8_EINVAL, "out_scale is NULL");
+  if (out_scale != nullptr && !aligned(out_scale, 4)) return fail(BNB8_EINVAL, "out_scale misaligned");
+  Plan plan;
+  rc = make_plan(tensors, ntensors, *hp, log2B, qmap1, qmap2, &plan);
+  if (rc != BNB8_OK) return rc;
+  if (hp->max_unorm > 0.0f && plan.all_blocks > kStaticScratchBlocks)
+    return fail(BNB8_EWORKSPACE,
+                "bnb8_unorm_static handles at most %lld blocks per call (this list has %lld); "
+                "use bnb8_unorm with a workspace",
+                (long long)kStaticScratchBlocks, (long long)plan.all_blocks);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (hp->max_unorm <= 0.0f || plan.chunks.empty()) {
+    const cudaError_t e = launch_fill(out_scale, ntensors, 1.0f, s);
+    return e == cudaSuccess ? BNB8_OK : cuda_fail(e, "unorm fill");
+  }
+  float2* partials = nullptr;
+  rc = static_scratch(&partials);
+  if (rc != BNB8_OK) return rc;
+  // every partial a call reads is written by the same call's pre-pass first,
+  // so the contents left by an earlier call need no clearing
+  const Scalars sc = make_scalars(*hp);
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s);
+}

@@ -26,7 +26,8 @@
  *     launch error; errors raised later by the device surface on the stream.
  *   - The caller owns every buffer.  The library allocates no device or host
  *     memory that outlives a call; scratch comes from a caller-provided
- *     workspace (bnb8_workspace_size).
+ *     workspace (bnb8_workspace_size).  The one exception is the fixed
+ *     scratch array behind bnb8_unorm_static (see there).
  *   - Pointers marked "device" must be device-accessible memory of the
  *     current device.  Calls are reentrant; calls on different streams that
  *     touch the same buffers race, as with any CUDA kernel.
@@ -224,6 +225,29 @@ int bnb8_step_ademamix(const bnb8_tensor* tensors, int ntensors, const bnb8_hpar
 int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
                const float* qmap1, const float* qmap2, float* out_scale, void* workspace,
                size_t workspace_bytes, struct CUstream_st* stream);
+
+/* bnb8_unorm without a workspace, for callers that cannot allocate device
+ * memory: for example code whose device memory is all handed out by a host
+ * framework's pool that must see every allocation, or a hot loop where a
+ * cudaMalloc / cudaFree would stall the device.  This entry point calls no
+ * allocator; its scratch (the per-block partial norms) is a fixed array of
+ * 262,144 blocks (2 MiB) compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  The paper has no
+ * counterpart: this is a deployment variant of bnb8_unorm.
+ *   Same arguments, results and errors as bnb8_unorm, minus the workspace.
+ *   A list with more than 262,144 blocks (over all tensors, at hp->blocksize)
+ *   is rejected with BNB8_EWORKSPACE.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture on the device.
+ *   All calls on a device share the one array, so calls whose work overlaps
+ *   on the GPU (different streams, no ordering between them) race and give
+ *   undefined results; calls on one stream, or otherwise ordered, are safe.
+ *   Each call writes every partial it reads before reading it, so whatever an
+ *   earlier call left in the array does not matter. */
+int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
+                      const float* qmap1, const float* qmap2, float* out_scale,
+                      struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

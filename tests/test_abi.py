@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 10
+    assert len(names) == 11
     assert sorted(bnb8.EXPORTS) == names
     for name in names:
         assert hasattr(L, name), name
