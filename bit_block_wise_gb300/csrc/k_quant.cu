@@ -56,17 +56,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_quantize(const __grid_constant_
     const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
     float x[8];
     load8<DT, true>(a.x, e0, valid, vec && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0, x);
-    float r[1];
-    r[0] = 0.0f;
+    uint32_t r[1] = {0u};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) r[0] = fmaxf(r[0], fabsf(x[j]));
-    group_reduce<1, true>(r, GT, glocal, sred, parity);
+    for (int j = 0; j < 8; ++j) r[0] = max(r[0], __float_as_uint(fabsf(x[j])));
+    group_max_bits<1>(r, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
     parity ^= 1;
     if (!active) continue;
-    const float amax = r[0];
+    const float amax = __uint_as_float(r[0]);
     const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
     uint32_t e[8];
-    if (fast_map && inv <= FLT_MAX) {
+    if (fast_map && r[0] <= 0x7f7fffffu && inv <= FLT_MAX) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) e[j] = encode_fast(x[j], inv, stbl + kTblZero);
     } else {

@@ -54,7 +54,7 @@ struct Step8Smem {
   static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
 };
 
-template <int OPT, int DT, int MODE>
+template <int OPT, int DT, int MODE, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ StepArgs a) {
   constexpr int NS = Traits<OPT>::NS;
   constexpr int NM = Traits<OPT>::NM;
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
     for (int m = 0; m < NM; ++m) build_table(smid + m * 256, stbl + m * kTblSize, &s_bad[m], &s_below, s_scan);
   }
-  bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
+  const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
 
   // ---- group geometry ----
   const int log2B = a.log2B;
@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   // warp-uniform loop base: the first group of this warp
   const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
+  // lanes of this thread's group inside its warp (GT < 32)
+  const uint32_t gmask = GT >= 32 ? 0xffffffffu : (((1u << GT) - 1u) << (in_warp * GT));
   int parity = 0;
 
   // parity selects the half of the reduction scratch; it flips after every
@@ -111,12 +113,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     const int64_t left = active ? d.n - e0 : 0;
     const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
     const bool vec = d.vec_ok != 0;
+    const bool full = vec && valid == 8;
     const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nblocks);
 
     float p[8], g[8];
     uint2 cw[NS];
     float am[NS];
-    if (MODE == MODE_STEP && a.skip_zeros) {
+    if (MODE == MODE_STEP && SKIP) {
       // skip_zeros: read g first; a block whose gradient is all zero is left
       // untouched, so its p, codes and absmax are never read.  Groups of fewer
       // than 32 threads skip only when their whole warp may.
@@ -128,10 +131,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       if (GT <= 32) {
         group_nz = __any_sync(0xffffffffu, nz);
       } else {
-        float v[1] = {nz ? 1.0f : 0.0f};
-        group_reduce<1, true>(v, GT, glocal, sred, parity);
+        uint32_t v[1] = {nz ? 1u : 0u};
+        group_max_bits<1>(v, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
         parity ^= 1;
-        group_nz = v[0] != 0.0f;
+        group_nz = v[0] != 0u;
       }
       if (!group_nz) continue;
       load8<DT, false>(d.p, e0, valid, vec, p);
@@ -147,23 +150,52 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     const float clip = (a.clip != nullptr && active) ? a.clip[d.index] : 1.0f;
     const float eff = a.step_size * clip;
 
+    // ---- dequantize, update; new states in s, running max of |s| in mx ----
     float s[NS][8];
+    uint32_t mx[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) mx[k] = 0u;
     float usq = 0.0f, psq = 0.0f;
     bool any = false;
+    if (full) {
+      // whole group of 8 present: no per-element predicates
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float st[3];
+      for (int j = 0; j < 8; ++j) {
+        float st[3];
 #pragma unroll
-      for (int k = 0; k < 3; ++k)
-        st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
-      if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
-      bool skipped = true;
-      float u = 0.0f;
-      if (j < valid) u = elem_update<OPT>(a, eff, p[j], g[j], st, skipped);
-      if (!skipped) any = true;
-      if (MODE == MODE_NORM) usq = usq + u * u;
+        for (int k = 0; k < 3; ++k)
+          st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
+        if (MODE == MODE_NORM) psq = psq + p[j] * p[j];
+        bool skipped;
+        const float u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+        if (SKIP) any = any || !skipped;
+        if (MODE == MODE_NORM) usq = usq + u * u;
 #pragma unroll
-      for (int k = 0; k < NS; ++k) s[k][j] = j < valid ? st[k] : 0.0f;
+        for (int k = 0; k < NS; ++k) {
+          s[k][j] = st[k];
+          mx[k] = max(mx[k], __float_as_uint(fabsf(st[k])));
+        }
+      }
+      if (!SKIP) any = true;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float st[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
+        if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
+        bool skipped = true;
+        float u = 0.0f;
+        if (j < valid) u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+        if (!skipped) any = true;
+        if (MODE == MODE_NORM) usq = usq + u * u;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          s[k][j] = j < valid ? st[k] : 0.0f;
+          mx[k] = max(mx[k], __float_as_uint(fabsf(s[k][j])));
+        }
+      }
     }
 
     if constexpr (MODE == MODE_NORM) {
@@ -174,27 +206,39 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       continue;
     }
 
-    // ---- new absmax per state (and whether anything changed) ----
-    float r[NS + 1];
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      float mx = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(s[k][j]));
-      r[k] = mx;
-    }
-    r[NS] = any ? 1.0f : 0.0f;
-    group_reduce<NS + 1, true>(r, GT, glocal, sred, parity);
-    parity ^= 1;
-    if (!active || r[NS] == 0.0f) continue;  // nothing updated: p, codes, absmax untouched
+    // p does not depend on the new absmax: store it now (skipped elements
+    // write back their unchanged bits; a group with nothing updated writes
+    // only when skip_zeros could not leave its warp early, with the same bits)
+    if (active && any) store8<DT>(d.p, e0, valid, vec, p);
 
-    store8<DT>(d.p, e0, valid, vec, p);
+    // ---- new absmax per state (bit patterns of non-negative values) ----
+    group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
+    parity ^= 1;
+    if (SKIP) {
+      // whether any element of the group was updated
+      bool group_any;
+      if (GT >= 32) {
+        group_any = __any_sync(0xffffffffu, any);
+        if (GT > 32) {
+          uint32_t v[1] = {group_any ? 1u : 0u};
+          group_max_bits<1>(v, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
+          parity ^= 1;
+          group_any = v[0] != 0u;
+        }
+      } else {
+        group_any = (__ballot_sync(0xffffffffu, any) & gmask) != 0u;
+      }
+      if (!group_any) continue;  // nothing updated: p, codes, absmax untouched
+    }
+    if (!active) continue;
+
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
       const int m = Traits<OPT>::map_of(k);
-      const float amax = r[k];
+      const float amax = __uint_as_float(mx[k]);
       const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
-      const bool fast = fast_map[m] && inv <= FLT_MAX;
+      // the table path needs a finite absmax and reciprocal (no NaN / inf)
+      const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
       uint32_t e[8];
       if (fast) {
         const uint32_t* tz = stbl + m * kTblSize + kTblZero;
@@ -214,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   }
 }
 
-template <int OPT, int DT, int MODE>
-cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
+template <int OPT, int DT, int MODE, bool SKIP>
+cudaError_t launch_step8_skip(const StepArgs& a, int grid, cudaStream_t s) {
   constexpr int bytes = Step8Smem<OPT, MODE>::kBytes;
   static unsigned configured = 0u;  // one bit per device: the attribute is per device
   int dev = 0;
@@ -223,22 +267,29 @@ cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const unsigned bit = 1u << (dev & 31);
   if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(k_step8<OPT, DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
+    e = cudaFuncSetAttribute(k_step8<OPT, DT, MODE, SKIP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  k_step8<OPT, DT, MODE><<<grid, kThreads, bytes, s>>>(a);
+  k_step8<OPT, DT, MODE, SKIP><<<grid, kThreads, bytes, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int OPT, int DT, int MODE>
+cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
+  return a.skip_zeros ? launch_step8_skip<OPT, DT, MODE, true>(a, grid, s)
+                      : launch_step8_skip<OPT, DT, MODE, false>(a, grid, s);
 }
 
 template <int OPT, int DT, int MODE>
 int ctas_step8_t() {
   constexpr int bytes = Step8Smem<OPT, MODE>::kBytes;
-  cudaFuncSetAttribute(k_step8<OPT, DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaFuncSetAttribute(k_step8<OPT, DT, MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       bytes);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_step8<OPT, DT, MODE>, kThreads, bytes) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_step8<OPT, DT, MODE, false>, kThreads,
+                                                    bytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
