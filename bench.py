@@ -403,7 +403,12 @@ def live_frac(wl, grads):
 
 def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no, tdt):
     """The same step through the public API with the gradient arriving from
-    pinned host memory and the updated parameter read back every step."""
+    pinned host memory and the updated parameter read back to pinned host
+    memory, every step.  Tensors are split at block boundaries into chunks
+    (blocks are independent) so that the upload of chunk i+1, the step on
+    chunk i and the read-back of chunk i-1 run concurrently on three streams.
+    max_unorm needs every block of a tensor before any update, so with it the
+    tensors are stepped whole."""
     import torch
     if wl.elements > (1 << 28):
         steps = max(2, min(args.steps, 5))
@@ -414,26 +419,50 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     for hg, ps in zip(host_g, params):
         hg.copy_(ps.g if ps.g is not None else torch.zeros_like(ps.p))
     dev_g = [torch.empty_like(ps.p) for ps in params]
+    for ps, dg in zip(params, dev_g):
+        ps.g = dg
+    chunks_per_tensor = 1 if wl.hp.get("max_unorm", 0.0) > 0 else 8
+    work = []  # (tensor index, element range, piece)
+    for i, ps in enumerate(params):
+        ranges, pieces = bnb8.split_blocks(ps, wl.blocksize, chunks_per_tensor)
+        work += [(i, r, pc) for r, pc in zip(ranges, pieces)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    start.record(s_in)
+    read_back = [None] * len(work)   # per chunk: its last read-back of p
     for _ in range(steps):
-        for dg, hg in zip(dev_g, host_g):
-            dg.copy_(hg, non_blocking=True)
-        for ps, dg in zip(params, dev_g):
-            ps.g = dg
         step_no[0] += 1
         hp = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=step_no[0], **wl.hp)
-        bnb8.step(params, hp, q1, q2, workspace=workspace if ws_bytes else None, stream=stream)
-        for hp_, ps in zip(host_p, params):
-            hp_.copy_(ps.p, non_blocking=True)
-    end.record(stream)
+        for c, (i, (lo, hi), piece) in enumerate(work):
+            with torch.cuda.stream(s_in):
+                dev_g[i][lo:hi].copy_(host_g[i][lo:hi], non_blocking=True)
+                up = torch.cuda.Event()
+                up.record(s_in)
+            stream.wait_event(up)
+            if read_back[c] is not None:      # p of this chunk is still being read back
+                stream.wait_event(read_back[c])
+            bnb8.step([piece], hp, q1, q2, workspace=workspace if ws_bytes else None,
+                      stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                host_p[i][lo:hi].copy_(piece.p, non_blocking=True)
+                read_back[c] = torch.cuda.Event()
+                read_back[c].record(s_out)
+        # the next step's uploads overwrite g: wait until this step consumed it
+        s_in.wait_stream(stream)
+    s_out.wait_stream(s_in)
+    end.record(s_out)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     esz = 4 if wl.dtype == "f32" else 2
     return {"value": round(wl.elements / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": wl.elements * esz, "d2h_bytes_per_step": wl.elements * esz,
-            "ms_per_step": round(ms, 4), "steps": steps}
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "pipeline": f"{len(work)} block-aligned chunks, upload / step / read-back on "
+                        "three streams"}
 
 
 # ---------------------------------------------------------------------------

@@ -303,6 +303,35 @@ def step(params, hp: HParams, qmap1, qmap2=None, workspace=None, stream=None):
         bnb8_step_1state(params, hp, qmap1, workspace, stream)
 
 
+def split_blocks(ps: ParamState, blocksize: int, nchunks: int):
+    """Split one tensor's descriptor into views at block boundaries.
+
+    Blocks are quantized independently, so updating the pieces one by one is
+    the same update as updating the whole tensor.  Works for the 1- and
+    2-state layouts; AdEMAMix keeps m1 and m2 stacked as [2, n], which a view
+    cannot split, so it is returned whole.  Returns (element ranges, pieces).
+    """
+    n = ps.p.numel()
+    if ps.s1.numel() == 2 * n:          # AdEMAMix: m1 and m2 stacked, 8- or 32-bit
+        return [(0, n)], [ps]
+    nb = (n + blocksize - 1) // blocksize
+    per = max(1, -(-nb // max(1, nchunks)))
+    ranges, pieces = [], []
+    for b0 in range(0, nb, per):
+        b1 = min(nb, b0 + per)
+        lo, hi = b0 * blocksize, min(n, b1 * blocksize)
+        cut = lambda t, a, b: None if t is None else t[a:b]
+        g = cut(ps.g, lo, hi)
+        if ps.state_bits == 8:
+            piece = ParamState(ps.p[lo:hi], g, ps.s1[lo:hi], cut(ps.s2, lo, hi),
+                               cut(ps.absmax1, b0, b1), cut(ps.absmax2, b0, b1), 8)
+        else:
+            piece = ParamState(ps.p[lo:hi], g, ps.s1[lo:hi], cut(ps.s2, lo, hi), None, None, 32)
+        ranges.append((lo, hi))
+        pieces.append(piece)
+    return ranges, pieces
+
+
 def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256):
     """Allocate the all-zero optimizer state of parameter p (codes of 0.0 in
     the signed / unsigned maps of bnb8_create_qmap, absmax 0)."""

@@ -54,6 +54,56 @@ struct Step8Smem {
   static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
 };
 
+// Requantize the NS new states of one group and store codes and absmax.
+// mx holds the group's absmax bit patterns.  Lane k of the group computes the
+// reciprocal of state k's absmax and shares it, so each reciprocal is issued
+// once per warp instead of once per state.
+template <int OPT>
+__device__ __forceinline__ void requantize_store(const float (&s)[Traits<OPT>::NS][8],
+                                                 const uint32_t (&mx)[Traits<OPT>::NS],
+                                                 const StatePtrs<OPT>& sp, int64_t e0,
+                                                 int64_t blk, int valid, bool vec, int gtid,
+                                                 int src_base, int lane, const bool (&fast_map)[2],
+                                                 const bool (&nonneg_map)[2],
+                                                 const uint32_t* stbl, const float* smid) {
+  constexpr int NS = Traits<OPT>::NS;
+  const int my_k = lane - src_base;
+  uint32_t mine = mx[0];
+#pragma unroll
+  for (int k = 1; k < NS; ++k)
+    if (my_k == k) mine = mx[k];
+  const float am_mine = __uint_as_float(mine);
+  const float inv_mine = am_mine > 0.0f ? __frcp_rn(am_mine) : 0.0f;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int m = Traits<OPT>::map_of(k);
+    const float amax = __uint_as_float(mx[k]);
+    const float inv = __shfl_sync(0xffffffffu, inv_mine, src_base + k);
+    // the table path needs a finite absmax and reciprocal (no NaN / inf)
+    const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
+    uint32_t e[8];
+    if (fast) {
+      const uint32_t* tz = stbl + m * kTblSize + kTblZero;
+      if (Traits<OPT>::nonneg(k) && nonneg_map[m]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = encode_fast_nonneg(s[k][j], inv, tz);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = encode_fast(s[k][j], inv, tz);
+      }
+    } else {
+      const float* md = smid + m * 256;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = encode_search(s[k][j] * inv, md);
+    }
+    // byte 2 of each e[j] is the code
+    const uint32_t lo = __byte_perm(__byte_perm(e[0], e[1], 0x0062u), __byte_perm(e[2], e[3], 0x0062u), 0x5410u);
+    const uint32_t hi = __byte_perm(__byte_perm(e[4], e[5], 0x0062u), __byte_perm(e[6], e[7], 0x0062u), 0x5410u);
+    store_codes(sp.c[k], e0, valid, vec, make_uint2(lo, hi));
+    if (gtid == 0) sp.a[k][blk] = amax;
+  }
+}
+
 template <int OPT, int DT, int MODE, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ StepArgs a) {
   constexpr int NS = Traits<OPT>::NS;
@@ -83,12 +133,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     for (int m = 0; m < NM; ++m) build_table(smid + m * 256, stbl + m * kTblSize, &s_bad[m], &s_below, s_scan);
   }
   const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
+  // the map's lowest level is its first (ascending maps)
+  const bool nonneg_map[2] = {sq[0] >= 0.0f, NM > 1 && sq[256] >= 0.0f};
 
   // ---- group geometry ----
   const int log2B = a.log2B;
-  const int B = 1 << log2B;
-  const int GT = B >> 3;                  // threads per block
+  const int64_t B = int64_t(1) << log2B;
+  const int GT = static_cast<int>(B >> 3);   // threads per block
   const int groups_per_cta = kThreads / GT;
+  const int groups_per_warp = GT < 32 ? 32 / GT : 1;
   const int lane = tid & 31;
   const int glocal = tid / GT;
   const int gtid = tid & (GT - 1);
@@ -96,164 +149,182 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   // warp-uniform loop base: the first group of this warp
   const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
+  const int src_base = in_warp * (GT < 32 ? GT : 0);  // first lane of this group in its warp
   // lanes of this thread's group inside its warp (GT < 32)
   const uint32_t gmask = GT >= 32 ? 0xffffffffu : (((1u << GT) - 1u) << (in_warp * GT));
-  int parity = 0;
-
   // parity selects the half of the reduction scratch; it flips after every
   // group reduction so that consecutive reductions never share a slot
-  for (int64_t base = warp_g0; base < a.total_blocks; base += stride) {
-    const int64_t gb = base + in_warp;
-    const bool active = gb < a.total_blocks;
-    const int t = active ? (a.ntensors > 1 ? find_tensor(a, gb) : 0) : 0;
+  int parity = 0;
+
+  // Tensors are visited in order; within a tensor this warp's groups take the
+  // blocks gb = base + in_warp, base stepping by the grid's group count, so
+  // every per-tensor value is loaded once.  A warp whose groups straddle a
+  // tensor boundary (blocks of fewer than 256 elements) visits that base once
+  // per tensor, with disjoint groups active.
+  for (int t = 0; t < a.ntensors; ++t) {
     const DevTensor& d = a.t[t];
-    const int64_t blk = active ? gb - d.first_block : 0;
-    const int64_t nblocks = (d.n + B - 1) >> log2B;
-    const int64_t e0 = (blk << log2B) + static_cast<int64_t>(gtid) * 8;
-    const int64_t left = active ? d.n - e0 : 0;
-    const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
+    const int64_t fb = d.first_block, n = d.n;
+    const int64_t nb = (n + B - 1) >> log2B;
+    const int64_t end = fb + nb;
+    const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nb);
     const bool vec = d.vec_ok != 0;
-    const bool full = vec && valid == 8;
-    const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nblocks);
+    const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
+    // first warp base whose groups can reach this tensor
+    const int64_t lo = fb - (groups_per_warp - 1);
+    int64_t base = warp_g0;
+    if (base < lo) base += ((lo - base + stride - 1) / stride) * stride;
 
-    float p[8], g[8];
-    uint2 cw[NS];
-    float am[NS];
-    if (MODE == MODE_STEP && SKIP) {
-      // skip_zeros: read g first; a block whose gradient is all zero is left
-      // untouched, so its p, codes and absmax are never read.  Groups of fewer
-      // than 32 threads skip only when their whole warp may.
-      load8<DT, true>(d.g, e0, valid, vec, g);
-      bool nz = false;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) nz = nz || (j < valid && g[j] != 0.0f);
-      bool group_nz;
-      if (GT <= 32) {
-        group_nz = __any_sync(0xffffffffu, nz);
-      } else {
-        uint32_t v[1] = {nz ? 1u : 0u};
-        group_max_bits<1>(v, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
-        parity ^= 1;
-        group_nz = v[0] != 0u;
-      }
-      if (!group_nz) continue;
-      load8<DT, false>(d.p, e0, valid, vec, p);
-    } else {
-      load8<DT, false>(d.p, e0, valid, vec, p);
-      load8<DT, true>(d.g, e0, valid, vec, g);
-    }
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      cw[k] = load_codes(sp.c[k], e0, valid, vec);
-      am[k] = active ? sp.a[k][blk] : 0.0f;
-    }
-    const float clip = (a.clip != nullptr && active) ? a.clip[d.index] : 1.0f;
-    const float eff = a.step_size * clip;
+    for (; base < end; base += stride) {
+      const int64_t blk = base + in_warp - fb;
+      const bool active = blk >= 0 && blk < nb;
+      const int64_t e0 = (blk << log2B) + static_cast<int64_t>(gtid) * 8;
+      const int64_t left = active ? n - e0 : 0;
+      const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
+      const bool full = vec && valid == 8;
 
-    // ---- dequantize, update; new states in s, running max of |s| in mx ----
-    float s[NS][8];
-    uint32_t mx[NS];
+      float p[8], g[8];
+      uint2 cw[NS];
+      float am[NS];
+      if (MODE == MODE_STEP && SKIP) {
+        // skip_zeros: read g first; a block whose gradient is all zero is left
+        // untouched, so its p, codes and absmax are never read.  Groups of
+        // fewer than 32 threads skip only when their whole warp may.
+        load8<DT, true>(d.g, e0, valid, vec, g);
+        bool nz = false;
 #pragma unroll
-    for (int k = 0; k < NS; ++k) mx[k] = 0u;
-    float usq = 0.0f, psq = 0.0f;
-    bool any = false;
-    if (full) {
-      // whole group of 8 present: no per-element predicates
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float st[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
-        if (MODE == MODE_NORM) psq = psq + p[j] * p[j];
-        bool skipped;
-        const float u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
-        if (SKIP) any = any || !skipped;
-        if (MODE == MODE_NORM) usq = usq + u * u;
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-          s[k][j] = st[k];
-          mx[k] = max(mx[k], __float_as_uint(fabsf(st[k])));
-        }
-      }
-      if (!SKIP) any = true;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float st[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
-        if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
-        bool skipped = true;
-        float u = 0.0f;
-        if (j < valid) u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
-        if (!skipped) any = true;
-        if (MODE == MODE_NORM) usq = usq + u * u;
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-          s[k][j] = j < valid ? st[k] : 0.0f;
-          mx[k] = max(mx[k], __float_as_uint(fabsf(s[k][j])));
-        }
-      }
-    }
-
-    if constexpr (MODE == MODE_NORM) {
-      float r[2] = {usq, psq};
-      group_reduce<2, false>(r, GT, glocal, sred, parity);
-      parity ^= 1;
-      if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
-      continue;
-    }
-
-    // p does not depend on the new absmax: store it now (skipped elements
-    // write back their unchanged bits; a group with nothing updated writes
-    // only when skip_zeros could not leave its warp early, with the same bits)
-    if (active && any) store8<DT>(d.p, e0, valid, vec, p);
-
-    // ---- new absmax per state (bit patterns of non-negative values) ----
-    group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
-    parity ^= 1;
-    if (SKIP) {
-      // whether any element of the group was updated
-      bool group_any;
-      if (GT >= 32) {
-        group_any = __any_sync(0xffffffffu, any);
-        if (GT > 32) {
-          uint32_t v[1] = {group_any ? 1u : 0u};
+        for (int j = 0; j < 8; ++j) nz = nz || (j < valid && g[j] != 0.0f);
+        bool group_nz;
+        if (GT <= 32) {
+          group_nz = __any_sync(0xffffffffu, nz);
+        } else {
+          uint32_t v[1] = {nz ? 1u : 0u};
           group_max_bits<1>(v, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
           parity ^= 1;
-          group_any = v[0] != 0u;
+          group_nz = v[0] != 0u;
         }
+        if (!group_nz) continue;
+        load8<DT, false>(d.p, e0, valid, vec, p);
       } else {
-        group_any = (__ballot_sync(0xffffffffu, any) & gmask) != 0u;
+        load8<DT, false>(d.p, e0, valid, vec, p);
+        load8<DT, true>(d.g, e0, valid, vec, g);
       }
-      if (!group_any) continue;  // nothing updated: p, codes, absmax untouched
-    }
-    if (!active) continue;
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        cw[k] = load_codes(sp.c[k], e0, valid, vec);
+        am[k] = active ? sp.a[k][blk] : 0.0f;
+      }
 
+      // ---- dequantize, update; new states in s, running max of |s| in mx ----
+      float s[NS][8];
+      uint32_t mx[NS];
 #pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      const int m = Traits<OPT>::map_of(k);
-      const float amax = __uint_as_float(mx[k]);
-      const float inv = amax > 0.0f ? __frcp_rn(amax) : 0.0f;
-      // the table path needs a finite absmax and reciprocal (no NaN / inf)
-      const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
-      uint32_t e[8];
-      if (fast) {
-        const uint32_t* tz = stbl + m * kTblSize + kTblZero;
+      for (int k = 0; k < NS; ++k) mx[k] = 0u;
+      float usq = 0.0f, psq = 0.0f;
+      bool any = false;
+      if (!SKIP && __all_sync(0xffffffffu, full)) {
+        // every thread of the warp holds 8 present, aligned elements: a
+        // straight-line path on packed pairs, no per-element predicates
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = encode_fast(s[k][j], inv, tz);
+        for (int j = 0; j < 8; j += 2) {
+          float2 st[3];
+#pragma unroll
+          for (int k = 0; k < 3; ++k)
+            st[k] = k < NS ? mul2(make_float2(sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)],
+                                              sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j + 1)]),
+                                  f2(am[k]))
+                           : f2(0.0f);
+          if (MODE == MODE_NORM) psq = psq + p[j] * p[j] + p[j + 1] * p[j + 1];
+          float2 pp = make_float2(p[j], p[j + 1]);
+          const float2 u = pair_update<OPT>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
+          p[j] = pp.x;
+          p[j + 1] = pp.y;
+          if (MODE == MODE_NORM) usq = usq + u.x * u.x + u.y * u.y;
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            s[k][j] = st[k].x;
+            s[k][j + 1] = st[k].y;
+            mx[k] = max(mx[k], max(__float_as_uint(fabsf(st[k].x)), __float_as_uint(fabsf(st[k].y))));
+          }
+        }
+        any = true;
+      } else if (full) {
+        // whole group of 8 present: no per-element predicates
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float st[3];
+#pragma unroll
+          for (int k = 0; k < 3; ++k)
+            st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
+          if (MODE == MODE_NORM) psq = psq + p[j] * p[j];
+          bool skipped;
+          const float u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          if (SKIP) any = any || !skipped;
+          if (MODE == MODE_NORM) usq = usq + u * u;
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            s[k][j] = st[k];
+            mx[k] = max(mx[k], __float_as_uint(fabsf(st[k])));
+          }
+        }
+        if (!SKIP) any = true;
       } else {
-        const float* md = smid + m * 256;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = encode_search(s[k][j] * inv, md);
+        for (int j = 0; j < 8; ++j) {
+          float st[3];
+#pragma unroll
+          for (int k = 0; k < 3; ++k)
+            st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
+          if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
+          bool skipped = true;
+          float u = 0.0f;
+          if (j < valid) u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          if (!skipped) any = true;
+          if (MODE == MODE_NORM) usq = usq + u * u;
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            s[k][j] = j < valid ? st[k] : 0.0f;
+            mx[k] = max(mx[k], __float_as_uint(fabsf(s[k][j])));
+          }
+        }
       }
-      // byte 2 of each e[j] is the code
-      const uint32_t lo = __byte_perm(__byte_perm(e[0], e[1], 0x0062u), __byte_perm(e[2], e[3], 0x0062u), 0x5410u);
-      const uint32_t hi = __byte_perm(__byte_perm(e[4], e[5], 0x0062u), __byte_perm(e[6], e[7], 0x0062u), 0x5410u);
-      store_codes(sp.c[k], e0, valid, vec, make_uint2(lo, hi));
-      if (gtid == 0) sp.a[k][blk] = amax;
+
+      if constexpr (MODE == MODE_NORM) {
+        float r[2] = {usq, psq};
+        group_reduce<2, false>(r, GT, glocal, sred, parity);
+        parity ^= 1;
+        if (active && gtid == 0) a.partials[fb + blk] = make_float2(r[0], r[1]);
+        continue;
+      }
+
+      // p does not depend on the new absmax: store it now (skipped elements
+      // write back their unchanged bits; a group with nothing updated writes
+      // only when skip_zeros could not leave its warp early, with the same
+      // bits)
+      if (active && any) store8<DT>(d.p, e0, valid, vec, p);
+
+      // ---- new absmax per state (bit patterns of non-negative values) ----
+      group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
+      parity ^= 1;
+      if (SKIP) {
+        // whether any element of the group was updated
+        bool group_any;
+        if (GT >= 32) {
+          group_any = __any_sync(0xffffffffu, any);
+          if (GT > 32) {
+            uint32_t v[1] = {group_any ? 1u : 0u};
+            group_max_bits<1>(v, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
+            parity ^= 1;
+            group_any = v[0] != 0u;
+          }
+        } else {
+          group_any = (__ballot_sync(0xffffffffu, any) & gmask) != 0u;
+        }
+        if (!group_any) continue;  // nothing updated: codes and absmax untouched
+      }
+      // every lane takes part (the reciprocals are shared by shuffle); only
+      // active lanes store
+      requantize_store<OPT>(s, mx, sp, e0, blk, active ? valid : 0, vec, active ? gtid : 1,
+                            src_base, lane, fast_map, nonneg_map, stbl, smid);
     }
   }
 }

@@ -326,22 +326,24 @@ static int decoupled(int optim) {
  * READING (update equations): the pages name torch's 32-bit optimizers as the
  * comparators ([P1] benchmark script: torch.optim.Adam / AdamW / SGD(lr,
  * momentum) / RMSprop(lr, alpha), Lion, the AdEMAMix reference) but print no
- * equations.  The textbook forms below reproduce those optimizers with zero
- * initial state.  Every operation is one binary32 rounding, in this order:
+ * equations and no operation order.  The textbook forms below reproduce those
+ * optimizers with zero initial state.  Every operation is one binary32
+ * rounding, in this order; fma(a, b, c) is IEEE 754 fusedMultiplyAdd (a*b+c
+ * rounded once), used wherever a product is added to something:
  *
  *   g  = g_raw * gnorm_scale;   coupled decay (Adam, Momentum, RMSprop,
- *                               Adagrad) when wd != 0:  g = g + wd * p
- *   Adam/AdamW: m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
+ *                               Adagrad) when wd != 0:  g = fma(wd, p, g)
+ *   Adam/AdamW: m = fma(b1, m, (1-b1)*g);  v = fma(b2, v, (1-b2)*(g*g))
  *               u = m / (sqrt(v) + eps_hat)
- *   Momentum:   m = b1*m + g;          u = m
- *   RMSprop:    v = b1*v + (1-b1)*(g*g);  u = g / (sqrt(v) + eps)
- *   Adagrad:    v = v + g*g;           u = g / (sqrt(v) + eps)
- *   Lion:       c = b1*m + (1-b1)*g;   u = sign(c);  m = b2*m + (1-b2)*g
- *   AdEMAMix:   m1 = b1*m1 + (1-b1)*g;  m2 = b3t*m2 + (1-b3t)*g;
- *               nu = b2*nu + (1-b2)*(g*g);
- *               u = (m1*inv_bc1 + alpha_t*m2) / (sqrt(nu) + eps_hat)
+ *   Momentum:   m = fma(b1, m, g);         u = m
+ *   RMSprop:    v = fma(b1, v, (1-b1)*(g*g));  u = g / (sqrt(v) + eps)
+ *   Adagrad:    v = fma(g, g, v);          u = g / (sqrt(v) + eps)
+ *   Lion:       c = fma(b1, m, (1-b1)*g);  u = sign(c);  m = fma(b2, m, (1-b2)*g)
+ *   AdEMAMix:   m1 = fma(b1, m1, (1-b1)*g);  m2 = fma(b3t, m2, (1-b3t)*g);
+ *               nu = fma(b2, nu, (1-b2)*(g*g));
+ *               u = fma(m1, inv_bc1, alpha_t*m2) / (sqrt(nu) + eps_hat)
  *   decoupled decay (AdamW, Lion, AdEMAMix) when wd != 0:  p = p * (1 - lr*wd)
- *   p = p - (step_size * clip) * u
+ *   p = fma(-(step_size * clip), u, p)
  *
  * [P3] skip_zeros: where the raw gradient is exactly zero the parameter and
  * the states keep their old values (tested before gnorm_scale and decay).
@@ -365,48 +367,48 @@ static elem_result update_element(const oracle_hparams* hp, const step_scalars* 
 
   float wd = hp->weight_decay;
   float g = g_raw * hp->gnorm_scale;
-  if (!decoupled(hp->optim) && wd != 0.0f) g = g + wd * p;
+  if (!decoupled(hp->optim) && wd != 0.0f) g = fmaf(wd, p, g);
 
   float u = 0.0f;
   switch (hp->optim) {
     case OR_ADAM:
     case OR_ADAMW: {
-      float m = sc->b1 * s_old[0] + sc->omb1 * g;
-      float v = sc->b2 * s_old[1] + sc->omb2 * (g * g);
+      float m = fmaf(sc->b1, s_old[0], sc->omb1 * g);
+      float v = fmaf(sc->b2, s_old[1], sc->omb2 * (g * g));
       u = m / (sqrtf(v) + sc->eps_hat);
       r.s[0] = m;
       r.s[1] = v;
       break;
     }
     case OR_MOMENTUM: {
-      float m = sc->b1 * s_old[0] + g;
+      float m = fmaf(sc->b1, s_old[0], g);
       u = m;
       r.s[0] = m;
       break;
     }
     case OR_RMSPROP: {
-      float v = sc->b1 * s_old[0] + sc->omb1 * (g * g);
+      float v = fmaf(sc->b1, s_old[0], sc->omb1 * (g * g));
       u = g / (sqrtf(v) + sc->eps_hat);
       r.s[0] = v;
       break;
     }
     case OR_ADAGRAD: {
-      float v = s_old[0] + g * g;
+      float v = fmaf(g, g, s_old[0]);
       u = g / (sqrtf(v) + sc->eps_hat);
       r.s[0] = v;
       break;
     }
     case OR_LION: {
-      float c = sc->b1 * s_old[0] + sc->omb1 * g;
+      float c = fmaf(sc->b1, s_old[0], sc->omb1 * g);
       u = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
-      r.s[0] = sc->b2 * s_old[0] + sc->omb2 * g;
+      r.s[0] = fmaf(sc->b2, s_old[0], sc->omb2 * g);
       break;
     }
     case OR_ADEMAMIX: {
-      float m1 = sc->b1 * s_old[0] + sc->omb1 * g;
-      float m2 = sc->b3t * s_old[1] + sc->omb3t * g;
-      float nu = sc->b2 * s_old[2] + sc->omb2 * (g * g);
-      u = (m1 * sc->inv_bc1 + sc->alpha_t * m2) / (sqrtf(nu) + sc->eps_hat);
+      float m1 = fmaf(sc->b1, s_old[0], sc->omb1 * g);
+      float m2 = fmaf(sc->b3t, s_old[1], sc->omb3t * g);
+      float nu = fmaf(sc->b2, s_old[2], sc->omb2 * (g * g));
+      u = fmaf(m1, sc->inv_bc1, sc->alpha_t * m2) / (sqrtf(nu) + sc->eps_hat);
       r.s[0] = m1;
       r.s[1] = m2;
       r.s[2] = nu;
@@ -416,7 +418,7 @@ static elem_result update_element(const oracle_hparams* hp, const step_scalars* 
       break;
   }
   if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;
-  r.p = p - step_eff * u;
+  r.p = fmaf(-step_eff, u, p);
   r.u = u;
   return r;
 }

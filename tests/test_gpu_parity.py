@@ -296,3 +296,29 @@ def test_step_unaligned_tensors(bnb8, qdev, optim):
 def test_ademamix_ragged_m2_offset(bnb8, qdev):
     # n % 8 != 0 puts the m2 codes of s1 = [2, n] off the 8-byte grid
     run_case(bnb8, qdev, "ademamix", "f32", 8, 256, [1003, 517], steps=3, seed=13)
+
+
+@pytest.mark.parametrize("optim", ["adam", "lion", "ademamix"])
+@pytest.mark.parametrize("bits", [8, 32])
+def test_split_blocks_pieces_equal_whole_tensor(bnb8, qdev, optim, bits):
+    # blocks are independent: updating block-aligned views one by one is the
+    # same update as updating the whole tensor (AdEMAMix 8-bit stays whole)
+    q1, q2 = map_pair(optim, S, U)
+    qd1 = qdev[0] if q1 is S else qdev[1]
+    qd2 = None if q2 is None else qdev[1]
+    n, B = 256 * 37 + 11, 256
+    st = random_state(optim, n, bits, B, 400, q1, q2)
+    p = workloads.normal(n, 0.1, 401)
+    g = to_dev(workloads.normal(n, 1e-2, 402))
+    whole = bnb8.ParamState(to_dev(p), g, *[to_dev(a) for a in st], bits)
+    split = bnb8.ParamState(to_dev(p), g, *[to_dev(a) for a in st], bits)
+    hp = bnb8.HParams(optim=optim, blocksize=B, step=2, weight_decay=1e-2, alpha=2.0)
+    bnb8.step([whole], hp, qd1, qd2)
+    _, pieces = bnb8.split_blocks(split, B, 5)
+    for pc in pieces:
+        bnb8.step([pc], hp, qd1, qd2)
+    torch.cuda.synchronize()
+    for name in ("p", "s1", "s2", "absmax1", "absmax2"):
+        a, b = getattr(whole, name), getattr(split, name)
+        if a is not None:
+            assert_same(name, to_host(b), to_host(a))

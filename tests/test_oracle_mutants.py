@@ -23,11 +23,11 @@ MUTANTS = [
     ("absmax of block 0 for every element", "return s->q[((const uint8_t*)s->base)[i]] * s->absmax[i / B];",
      "return s->q[((const uint8_t*)s->base)[i]] * s->absmax[0];",
      [(pins.test_8bit_step_tracks_32bit, ("adam", "f32"))]),
-    ("Adam m with beta2", "float m = sc->b1 * s_old[0] + sc->omb1 * g;\n      float v",
-     "float m = sc->b2 * s_old[0] + sc->omb2 * g;\n      float v",
+    ("Adam m with beta2", "float m = fmaf(sc->b1, s_old[0], sc->omb1 * g);\n      float v",
+     "float m = fmaf(sc->b2, s_old[0], sc->omb2 * g);\n      float v",
      [(pins.test_32bit_step_matches_torch_optim, ("adam", 0.0, 1.0))]),
-    ("Adam v not squared", "float v = sc->b2 * s_old[1] + sc->omb2 * (g * g);",
-     "float v = sc->b2 * s_old[1] + sc->omb2 * fabsf(g);",
+    ("Adam v not squared", "float v = fmaf(sc->b2, s_old[1], sc->omb2 * (g * g));",
+     "float v = fmaf(sc->b2, s_old[1], sc->omb2 * fabsf(g));",
      [(pins.test_32bit_step_matches_torch_optim, ("adam", 0.0, 1.0))]),
     ("Adam eps without bias correction", "sc->eps_hat = (float)(eps * sqrt(bc2));\n      sc->unorm_c = sqrt(bc2) / bc1;",
      "sc->eps_hat = (float)(eps);\n      sc->unorm_c = sqrt(bc2) / bc1;",
@@ -35,40 +35,40 @@ MUTANTS = [
     ("Adam step without sqrt(bc2)", "sc->step_size = (float)(lr * sqrt(bc2) / bc1);",
      "sc->step_size = (float)(lr / bc1);",
      [(pins.test_32bit_step_matches_torch_optim, ("adam", 0.0, 1.0))]),
-    ("coupled decay sign", "g = g + wd * p;", "g = g - wd * p;",
+    ("coupled decay sign", "g = fmaf(wd, p, g);", "g = fmaf(-wd, p, g);",
      [(pins.test_32bit_step_matches_torch_optim, ("adam", 1e-2, 1.0))]),
     ("decoupled decay dropped", "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;",
      "if (0) p = p * sc->decay;",
      [(pins.test_32bit_step_matches_torch_optim, ("adamw", 1e-2, 1.0))]),
     ("gnorm_scale ignored", "float g = g_raw * hp->gnorm_scale;", "float g = g_raw;",
      [(pins.test_32bit_step_matches_torch_optim, ("momentum", 0.0, 0.5))]),
-    ("momentum dampened", "float m = sc->b1 * s_old[0] + g;",
-     "float m = sc->b1 * s_old[0] + sc->omb1 * g;",
+    ("momentum dampened", "float m = fmaf(sc->b1, s_old[0], g);",
+     "float m = fmaf(sc->b1, s_old[0], sc->omb1 * g);",
      [(pins.test_32bit_step_matches_torch_optim, ("momentum", 0.0, 1.0))]),
-    ("RMSprop without (1-alpha)", "float v = sc->b1 * s_old[0] + sc->omb1 * (g * g);",
-     "float v = sc->b1 * s_old[0] + (g * g);",
+    ("RMSprop without (1-alpha)", "float v = fmaf(sc->b1, s_old[0], sc->omb1 * (g * g));",
+     "float v = fmaf(sc->b1, s_old[0], (g * g));",
      [(pins.test_32bit_step_matches_torch_optim, ("rmsprop", 0.0, 1.0))]),
-    ("Adagrad state not squared", "float v = s_old[0] + g * g;", "float v = s_old[0] + fabsf(g);",
+    ("Adagrad state not squared", "float v = fmaf(g, g, s_old[0]);", "float v = s_old[0] + fabsf(g);",
      [(pins.test_32bit_step_matches_torch_optim, ("adagrad", 0.0, 1.0))]),
-    ("Lion c with beta2", "float c = sc->b1 * s_old[0] + sc->omb1 * g;",
-     "float c = sc->b2 * s_old[0] + sc->omb2 * g;",
+    ("Lion c with beta2", "float c = fmaf(sc->b1, s_old[0], sc->omb1 * g);",
+     "float c = fmaf(sc->b2, s_old[0], sc->omb2 * g);",
      [(pins.test_lion_worked_example, ())]),
     ("Lion sign flipped", "u = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);",
      "u = c > 0.0f ? -1.0f : (c < 0.0f ? 1.0f : 0.0f);",
      [(pins.test_lion_worked_example, ())]),
-    ("Lion momentum with beta1", "r.s[0] = sc->b2 * s_old[0] + sc->omb2 * g;",
-     "r.s[0] = sc->b1 * s_old[0] + sc->omb1 * g;",
+    ("Lion momentum with beta1", "r.s[0] = fmaf(sc->b2, s_old[0], sc->omb2 * g);",
+     "r.s[0] = fmaf(sc->b1, s_old[0], sc->omb1 * g);",
      [(pins.test_lion_constant_gradient_closed_form, ())]),
-    ("AdEMAMix m2 with beta1", "float m2 = sc->b3t * s_old[1] + sc->omb3t * g;",
-     "float m2 = sc->b1 * s_old[1] + sc->omb1 * g;",
+    ("AdEMAMix m2 with beta1", "float m2 = fmaf(sc->b3t, s_old[1], sc->omb3t * g);",
+     "float m2 = fmaf(sc->b1, s_old[1], sc->omb1 * g);",
      [(pins.test_ademamix_constant_gradient_closed_form, ())]),
     ("AdEMAMix alpha on m1", "sc->alpha_t * m2", "sc->alpha_t * m1",
      [(pins.test_ademamix_constant_gradient_closed_form, ())]),
-    ("AdEMAMix m1 not bias-corrected", "(m1 * sc->inv_bc1 + sc->alpha_t * m2)",
+    ("AdEMAMix m1 not bias-corrected", "fmaf(m1, sc->inv_bc1, sc->alpha_t * m2)",
      "(m1 + sc->alpha_t * m2)",
      [(pins.test_ademamix_alpha_zero_is_adamw, ())]),
-    ("AdEMAMix nu with beta1", "float nu = sc->b2 * s_old[2] + sc->omb2 * (g * g);",
-     "float nu = sc->b1 * s_old[2] + sc->omb1 * (g * g);",
+    ("AdEMAMix nu with beta1", "float nu = fmaf(sc->b2, s_old[2], sc->omb2 * (g * g));",
+     "float nu = fmaf(sc->b1, s_old[2], sc->omb1 * (g * g));",
      [(pins.test_ademamix_alpha_zero_is_adamw, ())]),
     ("alpha warm-up inverted", "at = ramp < a ? ramp : a;", "at = ramp > a ? ramp : a;",
      [(pins.test_ademamix_schedules_endpoints_and_monotone, ())]),
@@ -92,9 +92,11 @@ MUTANTS = [
     ("parameter norm taken after the step", "psum += (double)pv * (double)pv;",
      "psum += (double)r.p * (double)r.p;",
      [(pins.test_max_unorm_norms_match_numpy, ())]),
-    ("clip applied to states too", "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = p - step_eff * u;",
-     "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = p - step_eff * u;\n  for (int j = 0; j < 3; ++j) r.s[j] *= step_eff / sc->step_size;",
+    ("clip applied to states too", "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = fmaf(-step_eff, u, p);",
+     "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = fmaf(-step_eff, u, p);\n  for (int j = 0; j < 3; ++j) r.s[j] *= step_eff / sc->step_size;",
      [(pins.test_max_unorm_invariants, ("momentum",))]),
+    ("parameter moves up the update", "r.p = fmaf(-step_eff, u, p);", "r.p = fmaf(step_eff, u, p);",
+     [(pins.test_32bit_step_matches_torch_optim, ("adam", 0.0, 1.0))]),
     ("bf16 rounds half up", "u += 0x7fffu + kept_lsb;", "u += 0x8000u;",
      [(pins.test_bf16_rounding_matches_torch, ())]),
     ("f16 subnormals truncated", "nearbyintf(fa * 16777216.0f)", "floorf(fa * 16777216.0f)",
