@@ -5,8 +5,9 @@
 A step is one optimizer update (one call of the library's step entry point)
 over the workload's synthetic parameters and gradients, which are resident in
 HBM before timing starts.  W untimed warm-up steps, then exactly K timed steps
-bracketed by a barrier and a device synchronize; the L2 cache is flushed
-(256 MiB written) before every timed step and each step is timed with CUDA
+bracketed by a barrier and a device synchronize; the L2 cache is flushed before
+every timed step (256 MiB written, then 256 MiB of other data read, so the
+step starts with clean, unrelated lines) and each step is timed with CUDA
 events on the launching stream.  Rank 0 prints one JSON line.
 
 Under torchrun (N > 1) every rank runs its own full replica of the workload
@@ -308,6 +309,15 @@ def run_gpu(args, wl):
                                                              **hp_kw))
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    flush_sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def flush_l2():
+        # write more than the L2 holds, then read as much other data: the L2
+        # ends up holding clean lines of unrelated buffers, so the timed step
+        # neither hits its own data nor pays for the flush's write-backs
+        flush.zero_()
+        torch.sum(flush_read, 0, dtype=torch.int64, out=flush_sink)
 
     step_no = [0]
 
@@ -336,7 +346,7 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         starts[k].record(stream)
         one_step(args.warmup + k)
         ends[k].record(stream)
@@ -368,7 +378,8 @@ def run_gpu(args, wl):
         "config": {"workload": wl.desc, "name": wl.name, "elements": wl.elements,
                    "tensors": len(wl.sizes), "blocksize": wl.blocksize, "optimizer": wl.optim,
                    "param_dtype": wl.dtype, "state": "uint8 codes + binary32 absmax",
-                   "l2": "flushed (256 MiB write) before every timed step",
+                   "l2": "flushed before every timed step (256 MiB written, then 256 MiB of "
+                         "other data read, leaving clean unrelated lines)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,

@@ -172,12 +172,13 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
 
 /* One optimizer update of every tensor in the list (host array of
  * descriptors; the list is read during the call only).
- * Per element, in binary32 (each operation rounded once, no FMA):
- *   g = g_raw * gnorm_scale; if coupled decay and wd != 0: g = g + wd * p
- *   Adam/AdamW  m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;
+ * Per element, in binary32, each operation rounded once; a product that is
+ * added (x*y + z below) is one fused multiply-add, rounded once:
+ *   g = g_raw * gnorm_scale; if coupled decay and wd != 0: g = wd*p + g
+ *   Adam/AdamW  m = b1*m + ((1-b1)*g);  v = b2*v + ((1-b2)*(g*g));
  *               u = m / (sqrt(v) + eps*sqrt(1-b2^t));  step = lr*sqrt(1-b2^t)/(1-b1^t)
  *   decoupled decay and wd != 0: p = p * (1 - lr*wd)
- *   p = p - (step * clip) * u
+ *   p = -(step * clip)*u + p
  * 8-bit states are dequantized (qmap[code] * absmax), updated, and
  * requantized with a fresh per-block absmax after p is written from the
  * unquantized new states.  skip_zeros and max_unorm as in bnb8_hparams.

@@ -2,9 +2,10 @@
 against the CPU oracle, element by element, on seeded inputs.
 
 Bar: codes and absmax bit-exact; parameters bit-exact too (the kernels run
-the oracle's binary32 operation sequence with IEEE division and square root
-and no FMA contraction), except where max_unorm's norm is summed in a
-different order: there p is within 1e-6 relative (binary32) / 1 ulp (16-bit).
+the oracle's binary32 operation sequence: IEEE division and square root,
+fused multiply-adds exactly where the update's definition has them and no
+other contraction), except where max_unorm's norm is summed in a different
+order: there p is within 1e-6 relative (binary32) / 1 ulp (16-bit).
 """
 import numpy as np
 import pytest
@@ -322,3 +323,36 @@ def test_split_blocks_pieces_equal_whole_tensor(bnb8, qdev, optim, bits):
         a, b = getattr(whole, name), getattr(split, name)
         if a is not None:
             assert_same(name, to_host(b), to_host(a))
+
+
+# ---------------------------------------------------------------------------
+# lists large enough that every CTA of the persistent grid visits many
+# blocks: warps cross from one tensor into the next, ragged last blocks,
+# tensors off the 16-byte grid next to aligned ones
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("optim,dtype", [("adam", "f32"), ("adamw", "bf16"), ("lion", "f32"),
+                                         ("rmsprop", "f16"), ("ademamix", "f32")])
+def test_step_many_blocks_per_cta(bnb8, qdev, optim, dtype):
+    # 8,001 blocks of 256 elements: about 26 per CTA of 304, crossing tensors
+    run_case(bnb8, qdev, optim, dtype, 8, 256, [256 * 5000 + 80, 256 * 3000], steps=2,
+             wd=1e-2, seed=21)
+
+
+@pytest.mark.parametrize("B", [64, 512, 4096])
+def test_step_blocksizes_many_blocks_per_cta(bnb8, qdev, B):
+    nblocks = 152 * (8192 // B) * 2 + 7
+    run_case(bnb8, qdev, "adam", "f32", 8, B, [nblocks * B - 3, 5 * B], steps=2, seed=22)
+
+
+def test_step_mixed_aligned_and_unaligned_tensors(bnb8, qdev):
+    # the middle tensor starts off the 16-byte grid (scalar path) between two
+    # aligned ones (vector path)
+    sizes = [256 * 2000, 256 * 1500 + 9, 256 * 2500]
+    run_case(bnb8, qdev, "adam", "f32", 8, 256, sizes, steps=2, offsets=[0, 1, 0], seed=23)
+
+
+def test_step_ademamix_second_moment_offset_many_blocks(bnb8, qdev):
+    # n % 16 != 0: m2's codes (n bytes into s1) are off the 16-byte grid
+    run_case(bnb8, qdev, "ademamix", "bf16", 8, 256, [256 * 3000 + 8, 256 * 2000], steps=2,
+             seed=24)
