@@ -412,14 +412,43 @@ def live_frac(wl, grads):
     return live / max(total, 1)
 
 
+def e2e_groups(bnb8, params, wl, ngroups):
+    """Work of one step in about ngroups launches: tensors larger than a
+    group's share are split at block boundaries (blocks are independent), and
+    consecutive pieces are packed into groups of about equal size.  With
+    max_unorm every tensor stays whole (its norm needs all of its blocks in
+    one call).  Returns a list of groups, each a list of
+    (tensor index, (lo, hi), piece)."""
+    target = -(-wl.elements // ngroups)
+    whole = wl.hp.get("max_unorm", 0.0) > 0
+    pieces = []
+    for i, ps in enumerate(params):
+        n = ps.p.numel()
+        k = 1 if whole else max(1, -(-n // target))
+        if k == 1:
+            pieces.append((i, (0, n), ps))
+        else:
+            ranges, pcs = bnb8.split_blocks(ps, wl.blocksize, k)
+            pieces += [(i, r, pc) for r, pc in zip(ranges, pcs)]
+    groups, cur, size = [], [], 0
+    for item in pieces:
+        cur.append(item)
+        size += item[1][1] - item[1][0]
+        if size >= target:
+            groups.append(cur)
+            cur, size = [], 0
+    if cur:
+        groups.append(cur)
+    return groups
+
+
 def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no, tdt):
     """The same step through the public API with the gradient arriving from
     pinned host memory and the updated parameter read back to pinned host
-    memory, every step.  Tensors are split at block boundaries into chunks
-    (blocks are independent) so that the upload of chunk i+1, the step on
-    chunk i and the read-back of chunk i-1 run concurrently on three streams.
-    max_unorm needs every block of a tensor before any update, so with it the
-    tensors are stepped whole."""
+    memory, every step.  The work is cut into four launches of about equal
+    size (e2e_groups), so that the upload of group i+1, the step on group i
+    and the read-back of group i-1 run concurrently on three streams; each
+    launch is a Stepper (arguments marshalled once)."""
     import torch
     if wl.elements > (1 << 28):
         steps = max(2, min(args.steps, 5))
@@ -432,36 +461,34 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     dev_g = [torch.empty_like(ps.p) for ps in params]
     for ps, dg in zip(params, dev_g):
         ps.g = dg
-    chunks_per_tensor = 1 if wl.hp.get("max_unorm", 0.0) > 0 else 8
-    work = []  # (tensor index, element range, piece)
-    for i, ps in enumerate(params):
-        ranges, pieces = bnb8.split_blocks(ps, wl.blocksize, chunks_per_tensor)
-        work += [(i, r, pc) for r, pc in zip(ranges, pieces)]
+    groups = e2e_groups(bnb8, params, wl, 4)
+    hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **wl.hp)
+    steppers = [bnb8.Stepper([pc for _, _, pc in grp], hp0, q1, q2,
+                             workspace=workspace if ws_bytes else None) for grp in groups]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in groups]
+    ev_done = [torch.cuda.Event() for _ in groups]
+    ev_back = [torch.cuda.Event() for _ in groups]
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
-    read_back = [None] * len(work)   # per chunk: its last read-back of p
-    for _ in range(steps):
+    for k in range(steps):
         step_no[0] += 1
-        hp = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=step_no[0], **wl.hp)
-        for c, (i, (lo, hi), piece) in enumerate(work):
+        for c, grp in enumerate(groups):
             with torch.cuda.stream(s_in):
-                dev_g[i][lo:hi].copy_(host_g[i][lo:hi], non_blocking=True)
-                up = torch.cuda.Event()
-                up.record(s_in)
-            stream.wait_event(up)
-            if read_back[c] is not None:      # p of this chunk is still being read back
-                stream.wait_event(read_back[c])
-            bnb8.step([piece], hp, q1, q2, workspace=workspace if ws_bytes else None,
-                      stream=stream)
-            ev = torch.cuda.Event()
-            ev.record(stream)
-            s_out.wait_event(ev)
+                for i, (lo, hi), _ in grp:
+                    dev_g[i][lo:hi].copy_(host_g[i][lo:hi], non_blocking=True)
+                ev_up[c].record(s_in)
+            stream.wait_event(ev_up[c])
+            if k > 0:                           # p of this group is still being read back
+                stream.wait_event(ev_back[c])
+            steppers[c](step_no[0], stream)
+            ev_done[c].record(stream)
+            s_out.wait_event(ev_done[c])
             with torch.cuda.stream(s_out):
-                host_p[i][lo:hi].copy_(piece.p, non_blocking=True)
-                read_back[c] = torch.cuda.Event()
-                read_back[c].record(s_out)
+                for i, (lo, hi), pc in grp:
+                    host_p[i][lo:hi].copy_(pc.p, non_blocking=True)
+                ev_back[c].record(s_out)
         # the next step's uploads overwrite g: wait until this step consumed it
         s_in.wait_stream(stream)
     s_out.wait_stream(s_in)
@@ -472,8 +499,8 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     return {"value": round(wl.elements / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": wl.elements * esz, "d2h_bytes_per_step": wl.elements * esz,
             "ms_per_step": round(ms, 4), "steps": steps,
-            "pipeline": f"{len(work)} block-aligned chunks, upload / step / read-back on "
-                        "three streams"}
+            "pipeline": f"{len(groups)} launches of about equal size, upload / step / read-back "
+                        "on three streams"}
 
 
 # ---------------------------------------------------------------------------

@@ -231,6 +231,8 @@ def bnb8_workspace_size(params: Sequence[ParamState], hp: HParams) -> int:
 
 def _workspace(params, hp, workspace):
     torch = _torch()
+    if hp.max_unorm == 0.0:
+        return None, 0  # the step entry points need no workspace then
     need = bnb8_workspace_size(params, hp)
     if need == 0:
         return None, 0
@@ -252,6 +254,39 @@ def _step(entry: str, params, hp: HParams, qmap1, qmap2, workspace, stream):
     else:
         _check(fn(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2), _ptr(ws),
                   ws_bytes, _stream(stream)))
+
+
+_ENTRY = {"adam": "bnb8_step_2state", "adamw": "bnb8_step_2state", "ademamix": "bnb8_step_ademamix",
+          "momentum": "bnb8_step_1state", "rmsprop": "bnb8_step_1state",
+          "adagrad": "bnb8_step_1state", "lion": "bnb8_step_1state"}
+
+
+class Stepper:
+    """The step entry point of hp.optim over a fixed tensor list, with the
+    arguments marshalled once: the descriptor array, the hyperparameter
+    struct, the workspace and the map pointers are built here, and each call
+    only sets the update number and the stream.  The tensors (and the
+    gradient tensors attached to them) must keep their storage while the
+    Stepper is used."""
+
+    def __init__(self, params, hp: HParams, qmap1, qmap2=None, workspace=None):
+        self.n = len(params)
+        self.arr = _tensor_array(params)
+        self.hc = hp.c(_dtype_code(params[0].p)) if params else None
+        self.ws, self.ws_bytes = _workspace(params, hp, workspace) if params else (None, 0)
+        self.entry = _ENTRY[hp.optim]
+        self.fn = getattr(lib(), self.entry)
+        if self.entry == "bnb8_step_1state":
+            self.args = (_ptr(qmap1), _ptr(self.ws), self.ws_bytes)
+        else:
+            self.args = (_ptr(qmap1), _ptr(qmap2), _ptr(self.ws), self.ws_bytes)
+        self.hp_ref = ctypes.byref(self.hc) if params else None
+
+    def __call__(self, step: int, stream=None):
+        if self.n == 0:
+            return
+        self.hc.step = int(step)
+        _check(self.fn(self.arr, self.n, self.hp_ref, *self.args, _stream(stream)))
 
 
 def bnb8_step_2state(params, hp: HParams, qmap1, qmap2, workspace=None, stream=None):

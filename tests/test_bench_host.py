@@ -91,3 +91,36 @@ def test_clock_summary():
 
 def test_traffic_is_null_for_other_kernel_sources(tmp_path, monkeypatch):
     assert bench.ncu_traffic("no-such-workload") is None
+
+
+@pytest.mark.parametrize("name,unorm", [("adam_4096", 0.0), ("gpt2xl", 0.0), ("gpt2xl", 1.0),
+                                        ("momentum_embedding", 0.0)])
+def test_e2e_groups_cover_every_element_once(name, unorm):
+    # the end-to-end pipeline's launches: every element of every tensor in
+    # exactly one piece, pieces block-aligned, whole tensors under max_unorm
+    import torch
+    import bit_block_wise_gb300 as bnb8
+    wl = bench.WORKLOADS[name]()
+    wl.hp = dict(wl.hp, max_unorm=unorm)
+    if name == "gpt2xl":   # a shortened list of the same shapes keeps host memory small
+        wl.sizes, wl.bits = wl.sizes[:40], wl.bits[:40]
+    params = []
+    for n, b in zip(wl.sizes, wl.bits):
+        p = torch.empty(n, dtype=torch.float32)
+        s1, s2, a1, a2 = bnb8.zero_state(p, wl.optim, b, wl.blocksize)
+        params.append(bnb8.ParamState(p, torch.empty_like(p), s1, s2, a1, a2, b))
+    groups = bench.e2e_groups(bnb8, params, wl, 4)
+    assert 1 <= len(groups) <= 5
+    covered = {i: [] for i in range(len(params))}
+    for grp in groups:
+        for i, (lo, hi), pc in grp:
+            assert pc.p.numel() == hi - lo
+            assert lo % wl.blocksize == 0
+            assert pc.p.data_ptr() == params[i].p.data_ptr() + 4 * lo
+            covered[i].append((lo, hi))
+    for i, ranges in covered.items():
+        ranges.sort()
+        assert ranges[0][0] == 0 and ranges[-1][1] == wl.sizes[i]
+        assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+        if unorm > 0:
+            assert len(ranges) == 1

@@ -356,3 +356,30 @@ def test_step_ademamix_second_moment_offset_many_blocks(bnb8, qdev):
     # n % 16 != 0: m2's codes (n bytes into s1) are off the 16-byte grid
     run_case(bnb8, qdev, "ademamix", "bf16", 8, 256, [256 * 3000 + 8, 256 * 2000], steps=2,
              seed=24)
+
+
+@pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
+def test_stepper_equals_step(bnb8, qdev, optim):
+    # arguments marshalled once, update number set per call: the same bits
+    # as the plain entry point, step after step
+    q1, q2 = map_pair(optim, S, U)
+    qd1 = qdev[0] if q1 is S else qdev[1]
+    qd2 = None if q2 is None else qdev[1]
+    sizes = [256 * 300 + 5, 4096]
+    a, b = [], []
+    for i, n in enumerate(sizes):
+        st = random_state(optim, n, 8, 256, 500 + i, q1, q2)
+        p = workloads.normal(n, 0.1, 510 + i)
+        g = to_dev(workloads.normal(n, 1e-2, 520 + i))
+        a.append(bnb8.ParamState(to_dev(p), g, *[to_dev(x) for x in st], 8))
+        b.append(bnb8.ParamState(to_dev(p), g, *[to_dev(x) for x in st], 8))
+    hp = dict(HP_BASE[optim], weight_decay=1e-2)
+    stepper = bnb8.Stepper(b, bnb8.HParams(optim=optim, step=1, **hp), qd1, qd2)
+    for k in range(1, 4):
+        bnb8.step(a, bnb8.HParams(optim=optim, step=k, **hp), qd1, qd2)
+        stepper(k)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        for name in ("p", "s1", "s2", "absmax1", "absmax2"):
+            if getattr(x, name) is not None:
+                assert_same(name, to_host(getattr(y, name)), to_host(getattr(x, name)))
