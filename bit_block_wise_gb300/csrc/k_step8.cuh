@@ -74,27 +74,56 @@ __device__ __forceinline__ void requantize_store(const float (&s)[Traits<OPT>::N
     if (my_k == k) mine = mx[k];
   const float am_mine = __uint_as_float(mine);
   const float inv_mine = am_mine > 0.0f ? __frcp_rn(am_mine) : 0.0f;
+  float inv[NS];
+  bool all_fast = true;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int m = Traits<OPT>::map_of(k);
+    inv[k] = __shfl_sync(0xffffffffu, inv_mine, src_base + k);
+    all_fast = all_fast && fast_map[m] && mx[k] <= 0x7f7fffffu && inv[k] <= FLT_MAX &&
+               (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
+  }
+  if (all_fast) {
+    // the usual case: every state takes the table path, in one straight-line
+    // block so that the lookups of all states overlap
+    uint32_t e[NS][8];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      const uint32_t* tz = stbl + Traits<OPT>::map_of(k) * kTblSize + kTblZero;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        e[k][j] = Traits<OPT>::nonneg(k) ? encode_fast_nonneg(s[k][j], inv[k], tz)
+                                         : encode_fast(s[k][j], inv[k], tz);
+    }
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      const uint32_t lo = __byte_perm(__byte_perm(e[k][0], e[k][1], 0x0062u), __byte_perm(e[k][2], e[k][3], 0x0062u), 0x5410u);
+      const uint32_t hi = __byte_perm(__byte_perm(e[k][4], e[k][5], 0x0062u), __byte_perm(e[k][6], e[k][7], 0x0062u), 0x5410u);
+      store_codes(sp.c[k], e0, valid, vec, make_uint2(lo, hi));
+      if (gtid == 0) sp.a[k][blk] = __uint_as_float(mx[k]);
+    }
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
     const int m = Traits<OPT>::map_of(k);
     const float amax = __uint_as_float(mx[k]);
-    const float inv = __shfl_sync(0xffffffffu, inv_mine, src_base + k);
     // the table path needs a finite absmax and reciprocal (no NaN / inf)
-    const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
+    const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv[k] <= FLT_MAX;
     uint32_t e[8];
     if (fast) {
       const uint32_t* tz = stbl + m * kTblSize + kTblZero;
       if (Traits<OPT>::nonneg(k) && nonneg_map[m]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = encode_fast_nonneg(s[k][j], inv, tz);
+        for (int j = 0; j < 8; ++j) e[j] = encode_fast_nonneg(s[k][j], inv[k], tz);
       } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = encode_fast(s[k][j], inv, tz);
+        for (int j = 0; j < 8; ++j) e[j] = encode_fast(s[k][j], inv[k], tz);
       }
     } else {
       const float* md = smid + m * 256;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) e[j] = encode_search(s[k][j] * inv, md);
+      for (int j = 0; j < 8; ++j) e[j] = encode_search(s[k][j] * inv[k], md);
     }
     // byte 2 of each e[j] is the code
     const uint32_t lo = __byte_perm(__byte_perm(e[0], e[1], 0x0062u), __byte_perm(e[2], e[3], 0x0062u), 0x5410u);

@@ -383,3 +383,75 @@ def test_stepper_equals_step(bnb8, qdev, optim):
         for name in ("p", "s1", "s2", "absmax1", "absmax2"):
             if getattr(x, name) is not None:
                 assert_same(name, to_host(getattr(y, name)), to_host(getattr(x, name)))
+
+
+# ---------------------------------------------------------------------------
+# maps other than the two dynamic maps: each kernel builds its search table
+# from the map it is given, so new contents in the same buffer, and many
+# different maps in a row, quantize exactly like the oracle
+# ---------------------------------------------------------------------------
+
+def _moved_levels(q, seed):
+    """q with five interior levels moved between their neighbours: still an
+    ascending map whose bucket search is exact, but a different table."""
+    rng = np.random.default_rng(seed)
+    q = q.copy()
+    for _ in range(5):
+        i = int(rng.integers(1, 255))
+        q[i] = np.float32(q[i - 1] + (q[i + 1] - q[i - 1]) * np.float32(rng.uniform(0.2, 0.8)))
+    return q
+
+
+def test_quantize_map_rewritten_in_place(bnb8):
+    x = _special_values(40 * 256 + 3, 31)
+    qd = to_dev(S.copy())
+    for k, q in enumerate([S, _moved_levels(S, 32), _moved_levels(S, 33), S]):
+        qd.copy_(to_dev(q))
+        codes, absmax = bnb8.bnb8_quantize_blockwise(to_dev(x), qd, 256)
+        oc, oa = oracle.quantize_blockwise(x, "f32", q, 256)
+        torch.cuda.synchronize()
+        assert_same(f"codes/{k}", to_host(codes), oc)
+        assert_same(f"absmax/{k}", to_host(absmax), oa)
+
+
+def test_quantize_many_different_maps(bnb8):
+    x = _special_values(9 * 256 + 100, 34)
+    maps_dev = []
+    for k in range(12):
+        q = _moved_levels(U if k % 2 else S, 35 + k)
+        qd = to_dev(q)
+        maps_dev.append(qd)
+        codes, absmax = bnb8.bnb8_quantize_blockwise(to_dev(x), qd, 128)
+        oc, oa = oracle.quantize_blockwise(x, "f32", q, 128)
+        torch.cuda.synchronize()
+        assert_same(f"codes/{k}", to_host(codes), oc)
+        assert_same(f"absmax/{k}", to_host(absmax), oa)
+
+
+@pytest.mark.parametrize("optim", ["adam", "lion"])
+def test_step_map_rewritten_in_place(bnb8, optim):
+    # the second step runs with new contents in the same map buffers
+    q1, q2 = map_pair(optim, S, U)
+    n, B = 256 * 50 + 7, 256
+    st = random_state(optim, n, 8, B, 40, q1, q2)
+    p = workloads.normal(n, 0.1, 41)
+    ref = oracle.TensorState(p.copy(), *[None if a is None else a.copy() for a in st], 8)
+    ps = bnb8.ParamState(to_dev(p), None, *[to_dev(a) for a in st], 8)
+    qd1 = to_dev(q1.copy())
+    qd2 = None if q2 is None else to_dev(q2.copy())
+    for k in range(1, 3):
+        if k == 2:
+            q1 = _moved_levels(q1, 42)
+            qd1.copy_(to_dev(q1))
+            if q2 is not None:
+                q2 = _moved_levels(q2, 43)
+                qd2.copy_(to_dev(q2))
+        g = workloads.normal(n, 1e-2, 44 + k)
+        ps.g = to_dev(g)
+        hp = dict(HP_BASE[optim], step=k, weight_decay=1e-2)
+        bnb8.step([ps], bnb8.HParams(optim=optim, **hp), qd1, qd2)
+        oracle.step(oracle.HParams(optim=optim, **hp), ref, g, "f32", B, q1, q2)
+        torch.cuda.synchronize()
+        for name in ("p", "s1", "s2", "absmax1", "absmax2"):
+            if getattr(ref, name) is not None:
+                assert_same(f"{optim}/step{k}/{name}", to_host(getattr(ps, name)), getattr(ref, name))
