@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quantize(const __grid_constant_
   __syncthreads();
   for (int i = tid; i < 256; i += kThreads) smid[i] = i < 255 ? (sq[i] + sq[i + 1]) * 0.5f : 0.0f;
   __syncthreads();
-  build_table(smid, stbl, &s_bad, &s_below, s_scan);
+  build_tables<1>(smid, stbl, &s_bad, &s_below, s_scan);
   const bool fast_map = s_bad == 0;
 
   const int log2B = a.log2B;

@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   uint32_t* stbl = reinterpret_cast<uint32_t*>(smem + L::kTbl);
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
   __shared__ int s_bad[2];
-  __shared__ int s_below;
-  __shared__ int s_scan[32];
+  __shared__ int s_below[2];
+  __shared__ int s_scan[2 * 32];
 
   const int tid = threadIdx.x;
   // ---- stage the maps, midpoints and (step mode) the bucket tables ----
@@ -158,8 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   }
   __syncthreads();
   if (MODE == MODE_STEP) {
-#pragma unroll
-    for (int m = 0; m < NM; ++m) build_table(smid + m * 256, stbl + m * kTblSize, &s_bad[m], &s_below, s_scan);
+    build_tables<NM>(smid, stbl, s_bad, s_below, s_scan);
   }
   const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
   // the map's lowest level is its first (ascending maps)
