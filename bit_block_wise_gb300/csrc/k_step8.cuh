@@ -55,31 +55,25 @@ struct Step8Smem {
 };
 
 // Requantize the NS new states of one group and store codes and absmax.
-// mx holds the group's absmax bit patterns.  Lane k of the group computes the
-// reciprocal of state k's absmax and shares it, so each reciprocal is issued
-// once per warp instead of once per state.
+// mx holds the group's absmax bit patterns.  Every lane computes the NS
+// reciprocals itself: independent of each other, they are shorter on the
+// critical path than one reciprocal followed by a shuffle.
 template <int OPT>
 __device__ __forceinline__ void requantize_store(const float (&s)[Traits<OPT>::NS][8],
                                                  const uint32_t (&mx)[Traits<OPT>::NS],
                                                  const StatePtrs<OPT>& sp, int64_t e0,
                                                  int64_t blk, int valid, bool vec, int gtid,
-                                                 int src_base, int lane, const bool (&fast_map)[2],
+                                                 const bool (&fast_map)[2],
                                                  const bool (&nonneg_map)[2],
                                                  const uint32_t* stbl, const float* smid) {
   constexpr int NS = Traits<OPT>::NS;
-  const int my_k = lane - src_base;
-  uint32_t mine = mx[0];
-#pragma unroll
-  for (int k = 1; k < NS; ++k)
-    if (my_k == k) mine = mx[k];
-  const float am_mine = __uint_as_float(mine);
-  const float inv_mine = am_mine > 0.0f ? __frcp_rn(am_mine) : 0.0f;
   float inv[NS];
   bool all_fast = true;
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
     const int m = Traits<OPT>::map_of(k);
-    inv[k] = __shfl_sync(0xffffffffu, inv_mine, src_base + k);
+    const float amk = __uint_as_float(mx[k]);
+    inv[k] = amk > 0.0f ? __frcp_rn(amk) : 0.0f;
     all_fast = all_fast && fast_map[m] && mx[k] <= 0x7f7fffffu && inv[k] <= FLT_MAX &&
                (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
   }
@@ -177,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   // warp-uniform loop base: the first group of this warp
   const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
-  const int src_base = in_warp * (GT < 32 ? GT : 0);  // first lane of this group in its warp
   // lanes of this thread's group inside its warp (GT < 32)
   const uint32_t gmask = GT >= 32 ? 0xffffffffu : (((1u << GT) - 1u) << (in_warp * GT));
   // parity selects the half of the reduction scratch; it flips after every
@@ -349,10 +342,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         }
         if (!group_any) continue;  // nothing updated: codes and absmax untouched
       }
-      // every lane takes part (the reciprocals are shared by shuffle); only
-      // active lanes store
+      // inactive lanes compute along (valid 0) and store nothing
       requantize_store<OPT>(s, mx, sp, e0, blk, active ? valid : 0, vec, active ? gtid : 1,
-                            src_base, lane, fast_map, nonneg_map, stbl, smid);
+                            fast_map, nonneg_map, stbl, smid);
     }
   }
 }
