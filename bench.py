@@ -310,14 +310,15 @@ def run_gpu(args, wl):
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
-    flush_sink = torch.empty((), dtype=torch.int64, device=device)
+    flush_sink = torch.empty((), dtype=torch.int32, device=device)
 
     def flush_l2():
-        # write more than the L2 holds, then read as much other data: the L2
+        # write more than the L2 holds, then read as much other data (a max
+        # reduction: it keeps the dtype, so it writes no temporary): the L2
         # ends up holding clean lines of unrelated buffers, so the timed step
         # neither hits its own data nor pays for the flush's write-backs
         flush.zero_()
-        torch.sum(flush_read, 0, dtype=torch.int64, out=flush_sink)
+        torch.amax(flush_read, 0, out=flush_sink)
 
     step_no = [0]
 
