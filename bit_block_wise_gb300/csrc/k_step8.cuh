@@ -195,6 +195,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     int64_t base = warp_g0;
     if (base < lo) base += ((lo - base + stride - 1) / stride) * stride;
 
+    // 1-state optimizers have the registers to load the next block's codes
+    // and absmax before this block's requantization (overlapping that
+    // latency with it); the others would spill
+    constexpr bool kAhead = MODE == MODE_STEP && !SKIP && NS == 1;
+    bool have_n = false;
+    uint2 cwn[NS];
+    float amn[NS];
     for (; base < end; base += stride) {
       const int64_t blk = base + in_warp - fb;
       const bool active = blk >= 0 && blk < nb;
@@ -231,8 +238,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       }
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
-        cw[k] = load_codes(sp.c[k], e0, valid, vec);
-        am[k] = active ? sp.a[k][blk] : 0.0f;
+        if (kAhead && have_n) {
+          cw[k] = cwn[k];
+          am[k] = amn[k];
+        } else {
+          cw[k] = load_codes(sp.c[k], e0, valid, vec);
+          am[k] = active ? sp.a[k][blk] : 0.0f;
+        }
       }
 
       // ---- dequantize, update; new states in s, running max of |s| in mx ----
@@ -322,6 +334,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       // only when skip_zeros could not leave its warp early, with the same
       // bits)
       if (active && any) store8<DT>(d.p, e0, valid, vec, p);
+      if (kAhead) {
+        // the next block of this tensor, when all 8 of this thread's elements
+        // exist there and its streams are aligned (else it loads as usual)
+        have_n = false;
+        const int64_t blk_n = base + stride + in_warp - fb;
+        if (vec && blk_n < nb) {
+          const int64_t e0n = (blk_n << log2B) + static_cast<int64_t>(gtid) * 8;
+          if (e0n + 8 <= n) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+              cwn[k] = load_codes(sp.c[k], e0n, 8, true);
+              amn[k] = sp.a[k][blk_n];
+            }
+            have_n = true;
+          }
+        }
+      }
 
       // ---- new absmax per state (bit patterns of non-negative values) ----
       group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
