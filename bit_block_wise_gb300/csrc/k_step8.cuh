@@ -195,10 +195,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     int64_t base = warp_g0;
     if (base < lo) base += ((lo - base + stride - 1) / stride) * stride;
 
-    // 1-state optimizers have the registers to load the next block's codes
-    // and absmax before this block's requantization (overlapping that
-    // latency with it); the others would spill
-    constexpr bool kAhead = MODE == MODE_STEP && !SKIP && NS == 1;
+    // Where the registers allow, the next block's absmax (2-state with
+    // binary32 p: Adam, AdamW) or codes and absmax (1-state) are loaded
+    // before this block's requantization, overlapping their latency with it;
+    // the other kernels would spill and keep the plain order
+    constexpr bool kAheadAm = MODE == MODE_STEP && !SKIP && (NS == 1 || (NS == 2 && DT == DT_F32));
+    constexpr bool kAheadCodes = MODE == MODE_STEP && !SKIP && NS == 1;
     bool have_n = false;
     uint2 cwn[NS];
     float amn[NS];
@@ -238,13 +240,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       }
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
-        if (kAhead && have_n) {
-          cw[k] = cwn[k];
-          am[k] = amn[k];
-        } else {
-          cw[k] = load_codes(sp.c[k], e0, valid, vec);
-          am[k] = active ? sp.a[k][blk] : 0.0f;
-        }
+        cw[k] = kAheadCodes && have_n ? cwn[k] : load_codes(sp.c[k], e0, valid, vec);
+        am[k] = kAheadAm && have_n ? amn[k] : (active ? sp.a[k][blk] : 0.0f);
       }
 
       // ---- dequantize, update; new states in s, running max of |s| in mx ----
@@ -334,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       // only when skip_zeros could not leave its warp early, with the same
       // bits)
       if (active && any) store8<DT>(d.p, e0, valid, vec, p);
-      if (kAhead) {
+      if (kAheadAm) {
         // the next block of this tensor, when all 8 of this thread's elements
         // exist there and its streams are aligned (else it loads as usual)
         have_n = false;
@@ -344,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
           if (e0n + 8 <= n) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
-              cwn[k] = load_codes(sp.c[k], e0n, 8, true);
+              if (kAheadCodes) cwn[k] = load_codes(sp.c[k], e0n, 8, true);
               amn[k] = sp.a[k][blk_n];
             }
             have_n = true;
