@@ -4,6 +4,7 @@
 // with -ffp-contract=off so every scalar below is one fixed expression.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -233,6 +234,12 @@ int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
     }
   }
   plan->all_blocks = offset;
+  // the 8-bit kernels index the blocks of one launch with 32-bit integers (a
+  // list that fits in HBM is far below the limit at B >= 64)
+  for (const Plan::Chunk& c : plan->chunks)
+    if (c.total_blocks > INT32_MAX)
+      return fail(BNB8_EUNSUPPORTED, "%lld blocks in one launch (at most %d)",
+                  static_cast<long long>(c.total_blocks), INT32_MAX);
   return BNB8_OK;
 }
 

@@ -167,9 +167,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   const int lane = tid & 31;
   const int glocal = tid / GT;
   const int gtid = tid & (GT - 1);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_cta;
+  // block indices of a launch fit in 32 bits (the host checks it)
+  const int32_t stride = static_cast<int32_t>(gridDim.x) * groups_per_cta;
   // warp-uniform loop base: the first group of this warp
-  const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
+  const int32_t warp_g0 = static_cast<int32_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
   // lanes of this thread's group inside its warp (GT < 32)
   const uint32_t gmask = GT >= 32 ? 0xffffffffu : (((1u << GT) - 1u) << (in_warp * GT));
@@ -184,15 +185,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   // per tensor, with disjoint groups active.
   for (int t = 0; t < a.ntensors; ++t) {
     const DevTensor& d = a.t[t];
-    const int64_t fb = d.first_block, n = d.n;
-    const int64_t nb = (n + B - 1) >> log2B;
-    const int64_t end = fb + nb;
+    const int32_t fb = static_cast<int32_t>(d.first_block);
+    const int64_t n = d.n;
+    const int32_t nb = static_cast<int32_t>((n + B - 1) >> log2B);
+    const int32_t end = fb + nb;
     const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nb);
     const bool vec = d.vec_ok != 0;
     const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
     // first warp base whose groups can reach this tensor
-    const int64_t lo = fb - (groups_per_warp - 1);
-    int64_t base = warp_g0;
+    const int32_t lo = fb - (groups_per_warp - 1);
+    int32_t base = warp_g0;
     if (base < lo) base += ((lo - base + stride - 1) / stride) * stride;
 
     // Where the registers allow, the next block's absmax (2-state with
@@ -205,9 +207,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     uint2 cwn[NS];
     float amn[NS];
     for (; base < end; base += stride) {
-      const int64_t blk = base + in_warp - fb;
+      const int32_t blk = base + in_warp - fb;
       const bool active = blk >= 0 && blk < nb;
-      const int64_t e0 = (blk << log2B) + static_cast<int64_t>(gtid) * 8;
+      const int64_t e0 = (static_cast<int64_t>(blk) << log2B) + gtid * 8;
       const int64_t left = active ? n - e0 : 0;
       const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
       const bool full = vec && valid == 8;
@@ -335,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         // the next block of this tensor, when all 8 of this thread's elements
         // exist there and its streams are aligned (else it loads as usual)
         have_n = false;
-        const int64_t blk_n = base + stride + in_warp - fb;
+        const int32_t blk_n = base + stride + in_warp - fb;
         if (vec && blk_n < nb) {
-          const int64_t e0n = (blk_n << log2B) + static_cast<int64_t>(gtid) * 8;
+          const int64_t e0n = (static_cast<int64_t>(blk_n) << log2B) + gtid * 8;
           if (e0n + 8 <= n) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {

@@ -161,3 +161,11 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bnb8, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         bnb8.lib()
+
+
+def test_launch_block_limit(L):
+    # the 8-bit kernels index one launch's blocks with 32-bit integers: a list
+    # beyond 2^31 - 1 blocks is refused before any device work
+    t = _tensor(n=(1 << 31) * 256 + 1)
+    assert _call2(L, [t], _hp()) == bnb8.BNB8_EUNSUPPORTED
+    assert b"blocks in one launch" in L.bnb8_last_error()
