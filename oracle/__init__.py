@@ -69,6 +69,7 @@ class _HParams(ctypes.Structure):
         ("t_alpha", ctypes.c_int64),
         ("t_beta3", ctypes.c_int64),
         ("skip_zeros", ctypes.c_int),
+        ("unorm_per_block", ctypes.c_int),
     ]
 
 
@@ -160,6 +161,8 @@ class HParams:
     max_unorm 0.0, skip_zeros False, alpha 0.0, t_alpha/t_beta3 None).
     ``beta3`` is AdEMAMix's third beta; ``gnorm_scale`` multiplies the raw
     gradient.  ``step`` is the 1-based number of the update being taken.
+    ``unorm_per_block`` takes max_unorm per block of ``blocksize`` elements
+    (one multiplier per block) instead of per tensor.
     """
     optim: str = "adam"
     lr: float = 1e-3
@@ -175,12 +178,13 @@ class HParams:
     t_alpha: int = 0
     t_beta3: int = 0
     skip_zeros: bool = False
+    unorm_per_block: bool = False
 
     def c(self) -> _HParams:
         return _HParams(OPTIMS[self.optim], self.lr, self.beta1, self.beta2, self.beta3,
                         self.alpha, self.eps, self.weight_decay, self.gnorm_scale,
                         self.max_unorm, int(self.step), int(self.t_alpha), int(self.t_beta3),
-                        int(bool(self.skip_zeros)))
+                        int(bool(self.skip_zeros)), int(bool(self.unorm_per_block)))
 
 
 def _ptr(a):

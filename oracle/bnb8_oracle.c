@@ -66,6 +66,7 @@ typedef struct {
   int64_t t_alpha;  /* AdEMAMix alpha warm-up length, 0 = no schedule */
   int64_t t_beta3;  /* AdEMAMix beta3 warm-up length, 0 = no schedule */
   int skip_zeros;
+  int unorm_per_block; /* max_unorm per quantization block instead of per tensor */
 } oracle_hparams;
 
 /* Per-step scalars, computed once in binary64 and rounded once to binary32. */
@@ -501,6 +502,29 @@ float oracle_unorm_scale(const oracle_hparams* hp, const void* p, const void* g,
   return 1.0f;
 }
 
+/* READING (the alternative, per block): the same test with U and P taken
+ * over one block of B elements (the quantization blocks of 8-bit states; the
+ * same partition of a tensor with 32-bit states), each block getting its own
+ * multiplier.  Elements lo..hi-1 of the tensor; sums in binary64, in element
+ * order. */
+static float block_unorm_scale(const oracle_hparams* hp, const step_scalars* sc, const void* p,
+                               const void* g, const state_ref* st, int ns, int state_bits,
+                               int dtype, int64_t B, int64_t lo, int64_t hi) {
+  double usum = 0.0, psum = 0.0;
+  for (int64_t i = lo; i < hi; ++i) {
+    float s_old[3] = {0.0f, 0.0f, 0.0f};
+    for (int j = 0; j < ns; ++j) s_old[j] = read_state(&st[j], state_bits, i, B);
+    float pv = load_elem(p, dtype, i);
+    elem_result r = update_element(hp, sc, sc->step_size, pv, load_elem(g, dtype, i), s_old);
+    usum += (double)r.u * (double)r.u;
+    psum += (double)pv * (double)pv;
+  }
+  double unorm = sc->unorm_c * sqrt(usum);
+  double limit = (double)hp->max_unorm * sqrt(psum);
+  if (hp->max_unorm > 0.0f && unorm > limit) return (float)(limit / unorm);
+  return 1.0f;
+}
+
 /* ---- the optimizer step on one tensor --------------------------------------
  * One update of parameter p with gradient g (same dtype) and its states.
  * 8-bit states: for every block, dequantize the old states (code -> q[code] *
@@ -522,8 +546,11 @@ float oracle_step_clipped(const oracle_hparams* hp, void* p, const void* g, void
                           int64_t B, const float* q1, const float* q2, float clip_in) {
   step_scalars sc;
   oracle_scalars(hp, &sc);
+  const int per_block = hp->unorm_per_block && hp->max_unorm > 0.0f;
   float clip = 1.0f;
-  if (clip_in >= 0.0f)
+  if (per_block)
+    clip = 1.0f; /* each block takes its own multiplier below */
+  else if (clip_in >= 0.0f)
     clip = clip_in; /* a multiplier the caller took from oracle_unorm_scale on the whole tensor */
   else if (hp->max_unorm > 0.0f)
     clip = oracle_unorm_scale(hp, p, g, s1, s2, absmax1, absmax2, n, state_bits, dtype, B, q1,
@@ -536,6 +563,11 @@ float oracle_step_clipped(const oracle_hparams* hp, void* p, const void* g, void
 
   if (state_bits == 32) {
     for (int64_t i = 0; i < n; ++i) {
+      if (per_block && i % B == 0) {
+        int64_t hi = i + B < n ? i + B : n;
+        step_eff = sc.step_size *
+                   block_unorm_scale(hp, &sc, p, g, st, ns, 32, dtype, B, i, hi);
+      }
       float s_old[3] = {0.0f, 0.0f, 0.0f};
       for (int j = 0; j < ns; ++j) s_old[j] = ((float*)st[j].base)[i];
       elem_result r =
@@ -556,6 +588,8 @@ float oracle_step_clipped(const oracle_hparams* hp, void* p, const void* g, void
   for (int64_t b = 0; b < nblocks; ++b) {
     int64_t lo = b * B, hi = lo + B < n ? lo + B : n;
     int any_update = 0;
+    if (per_block)
+      step_eff = sc.step_size * block_unorm_scale(hp, &sc, p, g, st, ns, 8, dtype, B, lo, hi);
     for (int64_t i = lo; i < hi; ++i) {
       float s_old[3] = {0.0f, 0.0f, 0.0f};
       for (int j = 0; j < ns; ++j) s_old[j] = read_state(&st[j], 8, i, B);

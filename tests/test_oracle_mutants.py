@@ -97,6 +97,13 @@ MUTANTS = [
      [(pins.test_max_unorm_invariants, ("momentum",))]),
     ("parameter moves up the update", "r.p = fmaf(-step_eff, u, p);", "r.p = fmaf(step_eff, u, p);",
      [(pins.test_32bit_step_matches_torch_optim, ("adam", 0.0, 1.0))]),
+    ("per-block clip over the whole tensor",
+     "block_unorm_scale(hp, &sc, p, g, st, ns, 8, dtype, B, lo, hi)",
+     "block_unorm_scale(hp, &sc, p, g, st, ns, 8, dtype, B, 0, n)",
+     [(pins.test_max_unorm_per_block_invariants, ("momentum", 8))]),
+    ("per-block parameter norm after the step", "    psum += (double)pv * (double)pv;\n  }\n  double unorm = sc->unorm_c",
+     "    psum += (double)r.p * (double)r.p;\n  }\n  double unorm = sc->unorm_c",
+     [(pins.test_max_unorm_per_block_invariants, ("adam", 8))]),
     ("bf16 rounds half up", "u += 0x7fffu + kept_lsb;", "u += 0x8000u;",
      [(pins.test_bf16_rounding_matches_torch, ())]),
     ("f16 subnormals truncated", "nearbyintf(fa * 16777216.0f)", "floorf(fa * 16777216.0f)",

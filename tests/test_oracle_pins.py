@@ -650,6 +650,84 @@ def test_max_unorm_norms_match_numpy():
     assert abs(scale - expect) <= 1e-6 * expect
 
 
+@pytest.mark.parametrize("optim,bits", [("adam", 8), ("momentum", 8), ("lion", 8),
+                                         ("adam", 32)])
+def test_max_unorm_per_block_invariants(optim, bits):
+    # the per-block reading: every block of B elements gets its own multiplier
+    q1, q2 = MAPS[optim]
+    n, B = 2000, 256
+    nb = (n + B - 1) // B
+    g = workloads.normal(n, 1e-2, 130)
+    if bits == 8:
+        s1, s2, a1, a2 = _random_8bit_state(optim, n, B, 131, q1, q2)
+    else:
+        s1 = workloads.normal(n, 1e-3, 131)
+        s2 = np.abs(workloads.normal(n, 1e-4, 132)) if oracle.NSTATES[optim] == 2 else None
+        a1 = a2 = None
+    base = oracle.TensorState(workloads.normal(n, 0.02, 133), s1, s2, a1, a2, bits)
+    hpkw = dict(optim=optim, step=3, lr=1e-3)
+
+    def block(t, b):
+        lo, hi = b * B, min(n, (b + 1) * B)
+        sl = lambda x: None if x is None else x[lo:hi]
+        am = lambda x: None if x is None else x[b:b + 1]
+        return oracle.TensorState(t.p[lo:hi].copy(), sl(t.s1).copy(),
+                                  None if t.s2 is None else sl(t.s2).copy(),
+                                  None if t.absmax1 is None else am(t.absmax1).copy(),
+                                  None if t.absmax2 is None else am(t.absmax2).copy(), bits)
+
+    # per-block norms, each block taken as a tensor of its own
+    U, P = np.zeros(nb), np.zeros(nb)
+    for b in range(nb):
+        _, U[b], P[b] = oracle.unorm_scale(oracle.HParams(max_unorm=1e30, **hpkw), block(base, b),
+                                           g[b * B:(b + 1) * B], "f32", B, q1, q2)
+    mu = float(np.median(U / P))   # about half of the blocks get clipped
+    plain, off, clip = base.copy(), base.copy(), base.copy()
+    oracle.step(oracle.HParams(**hpkw), plain, g, "f32", B, q1, q2)
+    oracle.step(oracle.HParams(max_unorm=0.0, unorm_per_block=True, **hpkw), off, g, "f32", B,
+                q1, q2)
+    oracle.step(oracle.HParams(max_unorm=mu, unorm_per_block=True, **hpkw), clip, g, "f32", B,
+                q1, q2)
+    np.testing.assert_array_equal(off.p, plain.p)
+    # clipping never touches the states
+    for name in ("s1", "s2", "absmax1", "absmax2"):
+        if getattr(plain, name) is not None:
+            np.testing.assert_array_equal(getattr(clip, name), getattr(plain, name))
+    sc = oracle.scalars(oracle.HParams(**hpkw))
+    clipped = 0
+    for b in range(nb):
+        lo, hi = b * B, min(n, (b + 1) * B)
+        dp = clip.p[lo:hi].astype(np.float64) - base.p[lo:hi].astype(np.float64)
+        dp0 = plain.p[lo:hi].astype(np.float64) - base.p[lo:hi].astype(np.float64)
+        if U[b] > np.float32(mu) * P[b]:
+            clipped += 1
+            applied = np.linalg.norm(dp) / sc["step_size"] * sc["unorm_c"]
+            assert abs(applied - np.float32(mu) * P[b]) <= 1e-3 * (mu * P[b]), b
+            assert dp.dot(dp0) / (np.linalg.norm(dp) * np.linalg.norm(dp0)) > 1 - 1e-6
+        else:
+            np.testing.assert_array_equal(clip.p[lo:hi], plain.p[lo:hi])
+    assert 0 < clipped < nb
+
+
+def test_max_unorm_per_block_equals_per_tensor_on_one_block():
+    # a tensor of one block: the two readings take the same norms
+    q1, q2 = MAPS["adam"]
+    n = B = 256
+    g = workloads.normal(n, 1e-2, 140)
+    s1, s2, a1, a2 = _random_8bit_state("adam", n, B, 141, q1, q2)
+    base = oracle.TensorState(workloads.normal(n, 0.02, 142), s1, s2, a1, a2, 8)
+    hpkw = dict(optim="adam", step=5, lr=1e-3, weight_decay=1e-2)
+    _, unorm, pnorm = oracle.unorm_scale(oracle.HParams(max_unorm=1e30, **hpkw), base, g, "f32",
+                                         B, q1, q2)
+    mu = 0.3 * unorm / pnorm
+    a, b = base.copy(), base.copy()
+    oracle.step(oracle.HParams(max_unorm=mu, **hpkw), a, g, "f32", B, q1, q2)
+    oracle.step(oracle.HParams(max_unorm=mu, unorm_per_block=True, **hpkw), b, g, "f32", B, q1, q2)
+    for x, y in zip((a.p, a.s1, a.s2, a.absmax1, a.absmax2), (b.p, b.s1, b.s2, b.absmax1, b.absmax2)):
+        np.testing.assert_array_equal(x, y)
+    assert not np.array_equal(a.p, base.p)
+
+
 # ---------------------------------------------------------------------------
 # checkpoint round trip (benchmark script: save/load the state every 10 steps;
 # raw codes and qmap must be identical after reload)
