@@ -87,10 +87,13 @@ MUTANTS = [
      [(pins.test_8bit_step_tracks_32bit, ("momentum", "f32"))]),
     ("AdEMAMix m2 aliases m1", "out[1].base = (char*)s1 + n * esz;", "out[1].base = (char*)s1;",
      [(pins.test_8bit_step_tracks_32bit, ("ademamix", "f32"))]),
-    ("update norm not squared", "usum += (double)r.u * (double)r.u;", "usum += fabs((double)r.u);",
+    ("update norm not squared",
+     "usum += (double)r.u * (double)r.u;\n    psum += (double)pv * (double)pv;\n  }\n  double unorm = sc.unorm_c",
+     "usum += fabs((double)r.u);\n    psum += (double)pv * (double)pv;\n  }\n  double unorm = sc.unorm_c",
      [(pins.test_max_unorm_norms_match_numpy, ())]),
-    ("parameter norm taken after the step", "psum += (double)pv * (double)pv;",
-     "psum += (double)r.p * (double)r.p;",
+    ("parameter norm taken after the step",
+     "psum += (double)pv * (double)pv;\n  }\n  double unorm = sc.unorm_c",
+     "psum += (double)r.p * (double)r.p;\n  }\n  double unorm = sc.unorm_c",
      [(pins.test_max_unorm_norms_match_numpy, ())]),
     ("clip applied to states too", "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = fmaf(-step_eff, u, p);",
      "if (decoupled(hp->optim) && wd != 0.0f) p = p * sc->decay;\n  r.p = fmaf(-step_eff, u, p);\n  for (int j = 0; j < 3; ++j) r.s[j] *= step_eff / sc->step_size;",
