@@ -76,9 +76,23 @@ class Workload:
             else:
                 rest = n * (2 * e + 8 * ns)                # p r+w, binary32 states r+w
             total += n * e + rest * live_block_frac        # g always read
-            if self.hp.get("max_unorm", 0.0) > 0:          # pre-pass reads g, p, states
+            if self.hp.get("max_unorm", 0.0) > 0 and not self.hp.get("unorm_per_block"):
+                # the per-tensor pre-pass reads g, p, states (per block: inside the step)
                 total += n * 2 * e + (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
         return int(total)
+
+
+def _cfg_unorm(per_block):
+    n = 4096 * 4096
+    how = "per block (inside the step)" if per_block else "per tensor (pre-pass + step)"
+    return Workload(
+        f"adam8bit_4096x4096_f32_B256_maxunorm_{'block' if per_block else 'tensor'}",
+        f"Adam8bit blockwise, one 4096x4096 float32 tensor, block 256, max_unorm 0.5 {how}, "
+        f"g ~ N(0,1e-3) with 1% N(0,1e-1) outliers, wd 1e-2",
+        "adam", "f32", [n], [8], 256,
+        dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2, max_unorm=0.5,
+             unorm_per_block=per_block),
+        ("outliers", 1e-3, 1e-1, 0.01))
 
 
 def _cfg_adam_4096(optim="adam", B=256):
@@ -132,6 +146,8 @@ WORKLOADS = {
                                           alpha=5.0, t_alpha=100, t_beta3=100, eps=1e-8),
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
+    "adam_4096_unorm": lambda: _cfg_unorm(False),
+    "adam_4096_unorm_block": lambda: _cfg_unorm(True),
 }
 DEFAULT_WORKLOAD = "adam_4096"
 
@@ -421,7 +437,7 @@ def e2e_groups(bnb8, params, wl, ngroups):
     one call).  Returns a list of groups, each a list of
     (tensor index, (lo, hi), piece)."""
     target = -(-wl.elements // ngroups)
-    whole = wl.hp.get("max_unorm", 0.0) > 0
+    whole = wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block")
     pieces = []
     for i, ps in enumerate(params):
         n = ps.p.numel()

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libbnb8.so")
 BNB8_OK, BNB8_EINVAL, BNB8_EUNSUPPORTED, BNB8_ECUDA, BNB8_EWORKSPACE = 0, 1, 2, 3, 4
 BNB8_F32, BNB8_BF16, BNB8_F16 = 0, 1, 2
 BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX = range(7)
+BNB8_UNORM_PER_BLOCK = 1
 
 OPTIMS = {"adam": BNB8_ADAM, "adamw": BNB8_ADAMW, "momentum": BNB8_MOMENTUM,
           "rmsprop": BNB8_RMSPROP, "adagrad": BNB8_ADAGRAD, "lion": BNB8_LION,
@@ -52,7 +53,7 @@ class Bnb8Hparams(ctypes.Structure):
                 ("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("beta3", ctypes.c_float), ("alpha", ctypes.c_float), ("eps", ctypes.c_float),
                 ("weight_decay", ctypes.c_float), ("gnorm_scale", ctypes.c_float),
-                ("max_unorm", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("max_unorm", ctypes.c_float), ("flags", ctypes.c_int32),
                 ("step", ctypes.c_int64), ("t_alpha", ctypes.c_int64),
                 ("t_beta3", ctypes.c_int64)]
 
@@ -148,11 +149,13 @@ class HParams:
     t_beta3: int = 0
     skip_zeros: bool = False
     blocksize: int = 256
+    unorm_per_block: bool = False  # max_unorm per block (BNB8_UNORM_PER_BLOCK)
 
     def c(self, dtype_code: int) -> Bnb8Hparams:
+        flags = BNB8_UNORM_PER_BLOCK if self.unorm_per_block else 0
         return Bnb8Hparams(OPTIMS[self.optim], dtype_code, self.blocksize, int(bool(self.skip_zeros)),
                            self.lr, self.beta1, self.beta2, self.beta3, self.alpha, self.eps,
-                           self.weight_decay, self.gnorm_scale, self.max_unorm, 0,
+                           self.weight_decay, self.gnorm_scale, self.max_unorm, flags,
                            int(self.step), int(self.t_alpha), int(self.t_beta3))
 
 

@@ -134,7 +134,8 @@ int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int*
   if (!valid_dtype(hp->dtype)) return fail(BNB8_EINVAL, "unknown dtype %d", hp->dtype);
   *log2B = log2_blocksize(hp->blocksize);
   if (*log2B < 0) return fail(BNB8_EINVAL, "blocksize %d is not a power of two in [64, 4096]", hp->blocksize);
-  if (hp->reserved != 0) return fail(BNB8_EINVAL, "hparams.reserved must be 0");
+  if ((hp->flags & ~BNB8_UNORM_PER_BLOCK) != 0)
+    return fail(BNB8_EINVAL, "hparams.flags: unknown bits 0x%x", hp->flags & ~BNB8_UNORM_PER_BLOCK);
   if (hp->step < 1) return fail(BNB8_EINVAL, "step must be >= 1 (got %lld)", (long long)hp->step);
   if (hp->t_alpha < 0 || hp->t_beta3 < 0) return fail(BNB8_EINVAL, "t_alpha / t_beta3 must be >= 0");
   if (!(hp->max_unorm >= 0.0f) || std::isinf(hp->max_unorm))
@@ -268,6 +269,8 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
   a.decay = sc.decay;
   a.wd = hp.weight_decay;
   a.gscale = hp.gnorm_scale;
+  a.max_unorm = hp.max_unorm;
+  a.unorm_c = static_cast<float>(sc.unorm_c);
   a.skip_zeros = hp.skip_zeros != 0;
   a.log2B = log2B;
   a.ntensors = static_cast<int32_t>(c.idx.size());
@@ -301,7 +304,7 @@ cudaError_t launch_family(int bits, int optim, int dtype, int mode, const StepAr
 }
 
 int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int log2B) {
-  static int cache[2][7][3][2] = {};
+  static int cache[2][7][3][3] = {};
   int& c = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
   if (c == 0) {
     if (optim == BNB8_ADAM || optim == BNB8_ADAMW) c = ctas_step_adam(bits, optim, dtype, mode);
@@ -357,7 +360,10 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
   if (plan.chunks.empty()) return BNB8_OK;
   const Scalars sc = make_scalars(*hp);
   const float* clip = nullptr;
-  if (hp->max_unorm > 0.0f) {
+  // per-block max_unorm: the norms are formed inside the step itself
+  const bool per_block = hp->max_unorm > 0.0f && (hp->flags & BNB8_UNORM_PER_BLOCK) != 0;
+  const int mode = per_block ? MODE_BCLIP : MODE_STEP;
+  if (hp->max_unorm > 0.0f && !per_block) {
     const size_t need = workspace_bytes_for(nt, plan.all_blocks);
     if (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)
       return fail(BNB8_EWORKSPACE, "max_unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
@@ -371,8 +377,8 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
   for (const Plan::Chunk& c : plan.chunks) {
     StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
     a.clip = clip;
-    const int grid = grid_for(c.bits, hp->optim, hp->dtype, MODE_STEP, c.total_blocks, log2B);
-    const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, MODE_STEP, a, grid, stream);
+    const int grid = grid_for(c.bits, hp->optim, hp->dtype, mode, c.total_blocks, log2B);
+    const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, mode, a, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "step launch");
   }
   return BNB8_OK;
@@ -476,7 +482,7 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
                             BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX};
   int log2B = 0;
   if (check_hparams(hp, all, 7, &log2B) != BNB8_OK) return 0;
-  if (hp->max_unorm <= 0.0f) return 0;
+  if (hp->max_unorm <= 0.0f || (hp->flags & BNB8_UNORM_PER_BLOCK) != 0) return 0;
   if (ntensors < 0 || (ntensors > 0 && tensors == nullptr)) {
     fail(BNB8_EINVAL, "bad tensor list");
     return 0;
@@ -524,6 +530,9 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
   int log2B = 0;
   int rc = check_hparams(hp, all, 7, &log2B);
   if (rc != BNB8_OK) return rc;
+  if ((hp->flags & BNB8_UNORM_PER_BLOCK) != 0)
+    return fail(BNB8_EINVAL, "the max_unorm pre-pass computes per-tensor multipliers; "
+                             "BNB8_UNORM_PER_BLOCK has none");
   if (ntensors > 0 && out_scale == nullptr) return fail(BNB8_EINVAL, "out_scale is NULL");
   if (out_scale != nullptr && !aligned(out_scale, 4)) return fail(BNB8_EINVAL, "out_scale misaligned");
   Plan plan;
@@ -587,6 +596,9 @@ extern "C" int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const
   int log2B = 0;
   int rc = check_hparams(hp, all, 7, &log2B);
   if (rc != BNB8_OK) return rc;
+  if ((hp->flags & BNB8_UNORM_PER_BLOCK) != 0)
+    return fail(BNB8_EINVAL, "the max_unorm pre-pass computes per-tensor multipliers; "
+                             "BNB8_UNORM_PER_BLOCK has none");
   if (ntensors > 0 && out_scale == nullptr) return fail(BNB8_EINVAL, "out_scale is NULL");
   if (out_scale != nullptr && !aligned(out_scale, 4)) return fail(BNB8_EINVAL, "out_scale misaligned");
   Plan plan;

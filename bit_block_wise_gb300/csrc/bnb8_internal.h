@@ -14,7 +14,9 @@ constexpr int kTblZero = 2946;      // entry of the smallest positive bucket
 
 enum Optim { ADAM = 0, ADAMW = 1, MOMENTUM = 2, RMSPROP = 3, ADAGRAD = 4, LION = 5, ADEMAMIX = 6 };
 enum Dtype { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
-enum Mode { MODE_STEP = 0, MODE_NORM = 1 };
+// MODE_STEP: the update; MODE_NORM: the per-tensor max_unorm pre-pass;
+// MODE_BCLIP: the update with max_unorm applied per block (no pre-pass).
+enum Mode { MODE_STEP = 0, MODE_NORM = 1, MODE_BCLIP = 2 };
 
 // One tensor of a launch.  Pointers are device pointers.
 struct DevTensor {
@@ -34,6 +36,7 @@ struct DevTensor {
 struct StepArgs {
   float b1, b2, b3t, omb1, omb2, omb3t;
   float step_size, eps_hat, inv_bc1, alpha_t, decay, wd, gscale;
+  float max_unorm, unorm_c;  // MODE_BCLIP: limit and |direction| = unorm_c * |u|
   int32_t skip_zeros;
   int32_t log2B;
   int32_t ntensors;

@@ -50,17 +50,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
 
     float usq = 0.0f, psq = 0.0f;
     bool any = false;
+    float ud[8];          // MODE_BCLIP: update directions, applied after the block's clip
+    uint32_t held = 0u;   // MODE_BCLIP: elements left as they are (skipped)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float st[3];
 #pragma unroll
       for (int k = 0; k < 3; ++k) st[k] = k < NS ? s[k][j] : 0.0f;
-      if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
+      if (MODE != MODE_STEP && j < valid) psq = psq + p[j] * p[j];
       bool skipped = true;
       float u = 0.0f;
-      if (j < valid) u = elem_update<OPT>(a, eff, p[j], g[j], st, skipped);
+      if (MODE == MODE_BCLIP) {
+        if (j < valid) u = elem_dir<OPT>(a, p[j], g[j], st, skipped);
+        ud[j] = u;
+        if (skipped) held |= 1u << j;
+      } else if (j < valid) {
+        u = elem_update<OPT>(a, eff, p[j], g[j], st, skipped);
+      }
       if (!skipped) any = true;
-      if (MODE == MODE_NORM) usq = usq + u * u;
+      if (MODE != MODE_STEP) usq = usq + u * u;
 #pragma unroll
       for (int k = 0; k < NS; ++k) s[k][j] = st[k];
     }
@@ -70,6 +78,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
       parity ^= 1;
       if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
       continue;
+    }
+    if constexpr (MODE == MODE_BCLIP) {
+      // max_unorm per block of B elements, as in the 8-bit kernel
+      float r[2] = {usq, psq};
+      group_reduce<2, false>(r, GT, glocal, sred, parity);
+      parity ^= 1;
+      const float unorm = a.unorm_c * sqrtf(r[0]);
+      const float limit = a.max_unorm * sqrtf(r[1]);
+      const float eff_b = eff * (unorm > limit ? limit / unorm : 1.0f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (!((held >> j) & 1u)) elem_apply<OPT>(a, eff_b, p[j], ud[j]);
     }
     if (!any) continue;  // every element skipped: leave them untouched
     store8<DT>(d.p, e0, valid, vec, p);

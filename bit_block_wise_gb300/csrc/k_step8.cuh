@@ -50,7 +50,7 @@ struct Step8Smem {
   static constexpr int kQ = 0;                                   // float q[NM][256]
   static constexpr int kMid = kQ + NM * 256 * 4;                 // float mid[NM][256]
   static constexpr int kTbl = kMid + NM * 256 * 4;               // uint32 tbl[NM][kTblSize]
-  static constexpr int kRed = kTbl + (MODE == MODE_STEP ? NM * kTblSize * 4 : 0);
+  static constexpr int kRed = kTbl + (MODE != MODE_NORM ? NM * kTblSize * 4 : 0);
   static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
 };
 
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     smid[i] = k < 255 ? (sq[m * 256 + k] + sq[m * 256 + k + 1]) * 0.5f : 0.0f;
   }
   __syncthreads();
-  if (MODE == MODE_STEP) {
+  if (MODE != MODE_NORM) {
     build_tables<NM>(smid, stbl, s_bad, s_below, s_scan);
   }
   const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       float p[8], g[8];
       uint2 cw[NS];
       float am[NS];
-      if (MODE == MODE_STEP && SKIP) {
+      if (MODE != MODE_NORM && SKIP) {
         // skip_zeros: read g first; a block whose gradient is all zero is left
         // untouched, so its p, codes and absmax are never read.  Groups of
         // fewer than 32 threads skip only when their whole warp may.
@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       for (int k = 0; k < NS; ++k) mx[k] = 0u;
       float usq = 0.0f, psq = 0.0f;
       bool any = false;
+      float ud[8];          // MODE_BCLIP: update directions, applied after the block's clip
+      uint32_t held = 0u;   // MODE_BCLIP: elements left as they are (skipped)
       if (!SKIP && __all_sync(0xffffffffu, full)) {
         // every thread of the warp holds 8 present, aligned elements: a
         // straight-line path on packed pairs, no per-element predicates
@@ -265,12 +267,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
                                               sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j + 1)]),
                                   f2(am[k]))
                            : f2(0.0f);
-          if (MODE == MODE_NORM) psq = psq + p[j] * p[j] + p[j + 1] * p[j + 1];
+          if (MODE != MODE_STEP) psq = psq + p[j] * p[j] + p[j + 1] * p[j + 1];
           float2 pp = make_float2(p[j], p[j + 1]);
-          const float2 u = pair_update<OPT>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
-          p[j] = pp.x;
-          p[j + 1] = pp.y;
-          if (MODE == MODE_NORM) usq = usq + u.x * u.x + u.y * u.y;
+          float2 u;
+          if (MODE == MODE_BCLIP) {
+            u = pair_dir<OPT>(a, pp, make_float2(g[j], g[j + 1]), st);
+            ud[j] = u.x;
+            ud[j + 1] = u.y;
+          } else {
+            u = pair_update<OPT>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
+            p[j] = pp.x;
+            p[j + 1] = pp.y;
+          }
+          if (MODE != MODE_STEP) usq = usq + u.x * u.x + u.y * u.y;
 #pragma unroll
           for (int k = 0; k < NS; ++k) {
             s[k][j] = st[k].x;
@@ -287,11 +296,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
           for (int k = 0; k < 3; ++k)
             st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
-          if (MODE == MODE_NORM) psq = psq + p[j] * p[j];
+          if (MODE != MODE_STEP) psq = psq + p[j] * p[j];
           bool skipped;
-          const float u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          float u;
+          if (MODE == MODE_BCLIP) {
+            u = elem_dir<OPT, SKIP>(a, p[j], g[j], st, skipped);
+            ud[j] = u;
+            if (skipped) held |= 1u << j;
+          } else {
+            u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          }
           if (SKIP) any = any || !skipped;
-          if (MODE == MODE_NORM) usq = usq + u * u;
+          if (MODE != MODE_STEP) usq = usq + u * u;
 #pragma unroll
           for (int k = 0; k < NS; ++k) {
             s[k][j] = st[k];
@@ -306,12 +322,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
           for (int k = 0; k < 3; ++k)
             st[k] = k < NS ? sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)] * am[k] : 0.0f;
-          if (MODE == MODE_NORM && j < valid) psq = psq + p[j] * p[j];
+          if (MODE != MODE_STEP && j < valid) psq = psq + p[j] * p[j];
           bool skipped = true;
           float u = 0.0f;
-          if (j < valid) u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          if (MODE == MODE_BCLIP) {
+            if (j < valid) u = elem_dir<OPT, SKIP>(a, p[j], g[j], st, skipped);
+            ud[j] = u;
+            if (skipped) held |= 1u << j;
+          } else if (j < valid) {
+            u = elem_update<OPT, SKIP>(a, eff, p[j], g[j], st, skipped);
+          }
           if (!skipped) any = true;
-          if (MODE == MODE_NORM) usq = usq + u * u;
+          if (MODE != MODE_STEP) usq = usq + u * u;
 #pragma unroll
           for (int k = 0; k < NS; ++k) {
             s[k][j] = j < valid ? st[k] : 0.0f;
@@ -326,6 +348,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         parity ^= 1;
         if (active && gtid == 0) a.partials[fb + blk] = make_float2(r[0], r[1]);
         continue;
+      }
+      if constexpr (MODE == MODE_BCLIP) {
+        // max_unorm per block: U = unorm_c * ||u||, P = ||p|| over the block
+        // (group sums as in the pre-pass); clip the step if U > max_unorm * P
+        float r[2] = {usq, psq};
+        group_reduce<2, false>(r, GT, glocal, sred, parity);
+        parity ^= 1;
+        const float unorm = a.unorm_c * sqrtf(r[0]);
+        const float limit = a.max_unorm * sqrtf(r[1]);
+        const float eff_b = eff * (unorm > limit ? limit / unorm : 1.0f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (!((held >> j) & 1u)) elem_apply<OPT>(a, eff_b, p[j], ud[j]);
       }
 
       // p does not depend on the new absmax: store it now (skipped elements

@@ -12,28 +12,40 @@ cudaError_t launch_step_1state(int bits, int optim, int dtype, int mode, const S
                                 int grid, cudaStream_t s) {
   BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(LION, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   return cudaErrorInvalidValue;
 }
 
@@ -45,28 +57,40 @@ cudaError_t launch_step_1state(int bits, int optim, int dtype, int mode, const S
 int ctas_step_1state(int bits, int optim, int dtype, int mode) {
   BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(MOMENTUM, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(RMSPROP, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(RMSPROP, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAGRAD, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(LION, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(LION, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   return 1;
 }
 

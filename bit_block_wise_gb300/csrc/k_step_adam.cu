@@ -12,16 +12,22 @@ cudaError_t launch_step_adam(int bits, int optim, int dtype, int mode, const Ste
                                 int grid, cudaStream_t s) {
   BNB8_DISPATCH(ADAM, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAM, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAM, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAM, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAM, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAM, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAM, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAM, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAM, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   return cudaErrorInvalidValue;
 }
 
@@ -33,16 +39,22 @@ cudaError_t launch_step_adam(int bits, int optim, int dtype, int mode, const Ste
 int ctas_step_adam(int bits, int optim, int dtype, int mode) {
   BNB8_DISPATCH(ADAM, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAM, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAM, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAM, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAM, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAM, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAM, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAM, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAM, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADAMW, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADAMW, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   return 1;
 }
 

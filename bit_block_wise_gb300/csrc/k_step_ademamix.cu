@@ -12,10 +12,13 @@ cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const
                                 int grid, cudaStream_t s) {
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
   return cudaErrorInvalidValue;
 }
 
@@ -27,10 +30,13 @@ cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const
 int ctas_step_ademamix(int bits, int optim, int dtype, int mode) {
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
   return 1;
 }
 

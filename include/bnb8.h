@@ -118,6 +118,14 @@ typedef struct bnb8_tensor {
  *   max_unorm   0 = off.  Otherwise, per tensor, if ||update direction|| >
  *               max_unorm * ||p|| the step is scaled down to that norm (a
  *               pre-pass over g, p and the states; needs a workspace).
+ *   flags       0, or BNB8_UNORM_PER_BLOCK: max_unorm taken per block of
+ *               blocksize elements instead of per tensor ("optim_overview.md":
+ *               the maximum value to normalize each block with, read
+ *               literally): each block whose ||update direction|| exceeds
+ *               max_unorm * ||p of the block|| is scaled down to it.  The
+ *               norms are formed inside the step (no pre-pass, no workspace);
+ *               the multiplier matches the binary64 definition to 1e-6.
+ *               Other bits: BNB8_EINVAL.
  *   step        1-based number of this update (bias corrections, schedules). */
 typedef struct bnb8_hparams {
   int32_t optim;
@@ -125,11 +133,15 @@ typedef struct bnb8_hparams {
   int32_t blocksize;
   int32_t skip_zeros;
   float lr, beta1, beta2, beta3, alpha, eps, weight_decay, gnorm_scale, max_unorm;
-  int32_t reserved; /* must be 0 */
+  int32_t flags; /* 0 or BNB8_UNORM_PER_BLOCK */
   int64_t step;
   int64_t t_alpha;
   int64_t t_beta3;
 } bnb8_hparams;
+
+enum bnb8_flags {
+  BNB8_UNORM_PER_BLOCK = 1 /* max_unorm per block instead of per tensor */
+};
 
 /* Message describing the last failure on this thread ("" if none). */
 const char* bnb8_last_error(void);
@@ -166,7 +178,7 @@ int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const f
                               struct CUstream_st* stream);
 
 /* Bytes of workspace the step functions and bnb8_unorm need for this tensor
- * list (0 when hp->max_unorm == 0 for the step functions).  Returns 0 and
+ * list (0 when hp->max_unorm == 0 or hp->flags has BNB8_UNORM_PER_BLOCK).  Returns 0 and
  * sets the error message on invalid arguments. */
 size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp);
 
@@ -215,7 +227,8 @@ int bnb8_step_ademamix(const bnb8_tensor* tensors, int ntensors, const bnb8_hpar
                        const float* qmap1, const float* qmap2, void* workspace,
                        size_t workspace_bytes, struct CUstream_st* stream);
 
-/* The max_unorm pre-pass on its own: writes, for every tensor i of the list,
+/* The max_unorm pre-pass on its own (per-tensor reading; hp->flags with
+ * BNB8_UNORM_PER_BLOCK is BNB8_EINVAL here): writes, for every tensor i of the list,
  * out_scale[i] (device binary32) = the step multiplier the update would use
  * (max_unorm * ||p|| / ||d|| if ||d|| > max_unorm * ||p||, else 1), where d
  * is the update direction of this step without lr and without decoupled

@@ -59,7 +59,7 @@ def test_create_qmap_null(L):
 def _hp(**kw):
     base = dict(optim=bnb8.BNB8_ADAM, dtype=bnb8.BNB8_F32, blocksize=256, skip_zeros=0, lr=1e-3,
                 beta1=0.9, beta2=0.999, beta3=0.9999, alpha=0.0, eps=1e-8, weight_decay=0.0,
-                gnorm_scale=1.0, max_unorm=0.0, reserved=0, step=1, t_alpha=0, t_beta3=0)
+                gnorm_scale=1.0, max_unorm=0.0, flags=0, step=1, t_alpha=0, t_beta3=0)
     base.update(kw)
     return bnb8.Bnb8Hparams(**base)
 
@@ -86,7 +86,7 @@ def _call2(L, tensors, hp, q1=FAKE, q2=FAKE, ws=None, wsb=0):
     (dict(dtype=7), b"dtype"),
     (dict(optim=bnb8.BNB8_LION), b"optimizer"),
     (dict(step=0), b"step"),
-    (dict(reserved=1), b"reserved"),
+    (dict(flags=2), b"flags"),
     (dict(max_unorm=-1.0), b"max_unorm"),
     (dict(max_unorm=float("nan")), b"max_unorm"),
     (dict(t_alpha=-1), b"t_alpha"),
@@ -138,6 +138,17 @@ def test_workspace_size_and_check(L):
     assert _call2(L, ts, hp, ws=FAKE, wsb=need - 1) == bnb8.BNB8_EWORKSPACE
     assert _call2(L, ts, hp, ws=FAKE + 8, wsb=need) == bnb8.BNB8_EWORKSPACE
     assert b"workspace" in L.bnb8_last_error()
+
+
+def test_per_block_unorm_needs_no_workspace(L):
+    ts = [_tensor(n=1000), _tensor(n=5, state_bits=32)]
+    arr = (bnb8.Bnb8Tensor * 2)(*ts)
+    hp = _hp(max_unorm=1.0, flags=bnb8.BNB8_UNORM_PER_BLOCK)
+    assert L.bnb8_workspace_size(arr, 2, ctypes.byref(hp)) == 0
+    # the per-tensor pre-pass entry points refuse it
+    assert L.bnb8_unorm(arr, 2, ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0, None) == bnb8.BNB8_EINVAL
+    assert b"per-tensor" in L.bnb8_last_error()
+    assert L.bnb8_unorm_static(arr, 2, ctypes.byref(hp), FAKE, FAKE, FAKE, None) == bnb8.BNB8_EINVAL
 
 
 def test_quantize_args_rejected(L):
