@@ -336,11 +336,17 @@ int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparam
     f.unorm_c = sc.unorm_c;
     f.max_unorm = hp.max_unorm;
     f.ntensors = a.ntensors;
+    int64_t chunks = 0;
     for (int k = 0; k < a.ntensors; ++k) {
       f.first_block[k] = a.t[k].first_block;
+      f.first_chunk[k] = chunks;
       f.index[k] = a.t[k].index;
+      const int64_t nb = (k + 1 < a.ntensors ? a.t[k + 1].first_block : c.total_blocks) -
+                         a.t[k].first_block;
+      chunks += (nb + kUnormChunk - 1) / kUnormChunk;
     }
     f.first_block[a.ntensors] = c.total_blocks;
+    f.first_chunk[a.ntensors] = chunks;
     e = launch_unorm_finalize(f, stream);
     if (e != cudaSuccess) return cuda_fail(e, "unorm finalize launch");
   }

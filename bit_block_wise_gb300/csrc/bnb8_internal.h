@@ -67,13 +67,21 @@ struct DequantArgs {
   int32_t log2B;
 };
 
+// The per-tensor max_unorm reduction of the pre-pass's block partials, in two
+// levels: k_unorm_chunks sums each chunk of kUnormChunk blocks of a tensor in
+// binary64 (one CTA per chunk) and writes the two sums in place over the
+// chunk's first two partials; k_unorm_finalize adds a tensor's chunk sums (a
+// one-block chunk keeps its binary32 partial) and writes the multiplier.
+constexpr int64_t kUnormChunk = 512;
+
 struct FinalizeArgs {
-  const float2* partials;
+  float2* partials;
   float* out_scale;        // indexed by DevTensor::index
   double unorm_c;          // |update direction| = unorm_c * |u|
   double max_unorm;
   int32_t ntensors;
   int64_t first_block[kMaxTensors + 1];
+  int64_t first_chunk[kMaxTensors + 1];  // chunks of tensors 0..t-1
   int32_t index[kMaxTensors];
 };
 
@@ -87,7 +95,7 @@ cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const
                                  int grid, cudaStream_t s);
 cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);  // both levels
 cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s);
 
 // Resident CTAs per SM of a step kernel (sizes the persistent grids).

@@ -102,17 +102,60 @@ __global__ void __launch_bounds__(256) k_dequantize(const __grid_constant__ Dequ
   }
 }
 
-// One CTA per tensor: sums the per-block partials of the max_unorm pre-pass
-// in binary64 (fixed order) and writes the step multiplier.
-__global__ void __launch_bounds__(256) k_unorm_finalize(const __grid_constant__ FinalizeArgs a) {
+// Level 1: one CTA per chunk of up to kUnormChunk blocks of one tensor.  Its
+// binary64 sums (sum u^2, sum p^2) in a fixed order (thread i takes blocks i,
+// i + 256, ...; then a tree) replace the chunk's first two partials.  Chunks
+// of a single block are left as they are.
+__global__ void __launch_bounds__(256) k_unorm_chunks(const __grid_constant__ FinalizeArgs a) {
   __shared__ double su[256], sp[256];
-  const int t = blockIdx.x;
-  const int64_t b0 = a.first_block[t], b1 = a.first_block[t + 1];
+  const int64_t c = blockIdx.x;
+  int t = 0;
+  while (t + 1 < a.ntensors && a.first_chunk[t + 1] <= c) ++t;
+  const int64_t b0 = a.first_block[t] + (c - a.first_chunk[t]) * kUnormChunk;
+  const int64_t b1 = b0 + kUnormChunk < a.first_block[t + 1] ? b0 + kUnormChunk : a.first_block[t + 1];
+  if (b1 - b0 < 2) return;
   double u = 0.0, p = 0.0;
   for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
     const float2 v = a.partials[b];
     u += static_cast<double>(v.x);
     p += static_cast<double>(v.y);
+  }
+  su[threadIdx.x] = u;
+  sp[threadIdx.x] = p;
+  __syncthreads();  // every partial of the chunk has been read
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      su[threadIdx.x] += su[threadIdx.x + o];
+      sp[threadIdx.x] += sp[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double* out = reinterpret_cast<double*>(a.partials + b0);
+    out[0] = su[0];
+    out[1] = sp[0];
+  }
+}
+
+// Level 2: one CTA per tensor adds the tensor's chunk sums in chunk order and
+// writes the step multiplier.
+__global__ void __launch_bounds__(256) k_unorm_finalize(const __grid_constant__ FinalizeArgs a) {
+  __shared__ double su[256], sp[256];
+  const int t = blockIdx.x;
+  const int64_t nchunks = a.first_chunk[t + 1] - a.first_chunk[t];
+  double u = 0.0, p = 0.0;
+  for (int64_t c = threadIdx.x; c < nchunks; c += blockDim.x) {
+    const int64_t b0 = a.first_block[t] + c * kUnormChunk;
+    const int64_t b1 = b0 + kUnormChunk < a.first_block[t + 1] ? b0 + kUnormChunk : a.first_block[t + 1];
+    if (b1 - b0 >= 2) {
+      const double* in = reinterpret_cast<const double*>(a.partials + b0);
+      u += in[0];
+      p += in[1];
+    } else {
+      const float2 v = a.partials[b0];
+      u += static_cast<double>(v.x);
+      p += static_cast<double>(v.y);
+    }
   }
   su[threadIdx.x] = u;
   sp[threadIdx.x] = p;
@@ -177,6 +220,12 @@ cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStr
 }
 
 cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s) {
+  const int64_t chunks = a.first_chunk[a.ntensors];
+  if (chunks > 0) {
+    k_unorm_chunks<<<static_cast<unsigned>(chunks), 256, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   k_unorm_finalize<<<a.ntensors, 256, 0, s>>>(a);
   return cudaGetLastError();
 }

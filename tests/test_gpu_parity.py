@@ -285,6 +285,29 @@ def test_unorm_scales_match_oracle(bnb8, qdev, optim):
         assert got[i] < 1.0
 
 
+def test_unorm_scales_chunked_sums(bnb8, qdev):
+    # the per-tensor sums go through chunks of 512 blocks: a one-block
+    # tensor, tensors whose last chunk is one block (the second one ragged)
+    q1, q2 = S, U
+    sizes = [100, 256 * 4097, 256 * 8192 + 5]
+    params, refs = [], []
+    for i, n in enumerate(sizes):
+        p = workloads.normal(n, 0.02, 150 + i)
+        st = random_state("adam", n, 8, 256, 160 + i, q1, q2)
+        refs.append(oracle.TensorState(p.copy(), *st, 8))
+        params.append(bnb8.ParamState(to_dev(p), to_dev(workloads.normal(n, 1e-2, 170 + i)),
+                                      *[to_dev(a) for a in st], 8))
+    hp = dict(HP_BASE["adam"], max_unorm=0.02, step=3)
+    scales = bnb8.bnb8_unorm(params, bnb8.HParams(optim="adam", **hp), qdev[0], qdev[1])
+    torch.cuda.synchronize()
+    got = to_host(scales)
+    for i, (ps, r) in enumerate(zip(params, refs)):
+        want, _, _ = oracle.unorm_scale(oracle.HParams(optim="adam", **hp), r, to_host(ps.g),
+                                        "f32", 256, q1, q2)
+        assert abs(got[i] - want) <= 1e-6 * want, (i, got[i], want)
+        assert got[i] < 1.0
+
+
 def test_step_multi_tensor_list_over_launch_capacity(bnb8, qdev):
     # more tensors than one launch carries, mixed 8/32-bit, empty tensors
     rng = np.random.default_rng(9)
