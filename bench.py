@@ -70,7 +70,11 @@ class Workload:
         ns, B = self.nstates(), self.blocksize
         total = 0.0
         for n, b in zip(self.sizes, self.bits):
-            nb = (n + B - 1) // B
+            nb = 1 if B == 0 else (n + B - 1) // B
+            if b == 8 and B == 0:
+                # tensor-wise: a first pass reads p, g and the codes for the
+                # new absmax, the second is the step
+                total += n * 2 * e + n * ns
             if b == 8:
                 rest = n * (2 * e + 2 * ns) + nb * 8 * ns  # p r+w, codes r+w, absmax r+w
             else:
@@ -97,10 +101,11 @@ def _cfg_unorm(per_block):
 
 def _cfg_adam_4096(optim="adam", B=256):
     n = 4096 * 4096
+    kind = f"blockwise, block {B}" if B else "tensor-wise (one absmax per state per tensor)"
     return Workload(
-        f"{optim}8bit_4096x4096_f32_B{B}",
-        f"{'Adam' if optim == 'adam' else 'AdamW'}8bit blockwise, one 4096x4096 float32 tensor "
-        f"(16,777,216 elements), block {B}, g ~ N(0,1e-3) with 1% N(0,1e-1) outliers, wd 1e-2",
+        f"{optim}8bit_4096x4096_f32_{'B%d' % B if B else 'tensorwise'}",
+        f"{'Adam' if optim == 'adam' else 'AdamW'}8bit {kind}, one 4096x4096 float32 tensor "
+        f"(16,777,216 elements), g ~ N(0,1e-3) with 1% N(0,1e-1) outliers, wd 1e-2",
         optim, "f32", [n], [8], B,
         dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2),
         ("outliers", 1e-3, 1e-1, 0.01))
@@ -146,6 +151,7 @@ WORKLOADS = {
                                           alpha=5.0, t_alpha=100, t_beta3=100, eps=1e-8),
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
+    "adam_4096_tensorwise": lambda: _cfg_adam_4096(B=0),
     "adam_4096_unorm": lambda: _cfg_unorm(False),
     "adam_4096_unorm_block": lambda: _cfg_unorm(True),
 }
@@ -437,7 +443,8 @@ def e2e_groups(bnb8, params, wl, ngroups):
     one call).  Returns a list of groups, each a list of
     (tensor index, (lo, hi), piece)."""
     target = -(-wl.elements // ngroups)
-    whole = wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block")
+    whole = (wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block")) or \
+        wl.blocksize == 0
     pieces = []
     for i, ps in enumerate(params):
         n = ps.p.numel()
@@ -523,12 +530,23 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
+def _gran(wl):
+    """Sample granularity (elements) of the oracle legs: the block size, or
+    256 for tensor-wise quantization (where the sample is one block)."""
+    return wl.blocksize or 256
+
+
+def _oracle_b(wl, n):
+    """The oracle's block size for a sample of n elements."""
+    return wl.blocksize or n
+
+
 def _oracle_sample(wl, n_sample, params=None):
     """Host copies of the first n_sample elements of the workload's first
     tensor (device state when given, else fresh seeded values)."""
     import oracle
     n = min(n_sample, wl.sizes[0])
-    B = wl.blocksize
+    B = _oracle_b(wl, n)
     dt = wl.dtype
     p = oracle.to_storage(workloads.normal(n, wl.p_std, 1), dt)
     q1 = oracle.create_qmap(wl.optim not in ("rmsprop", "adagrad"))
@@ -555,8 +573,8 @@ def time_oracle(wl, n_sample, steps, budget_s):
     done = 0
     t0 = time.perf_counter()
     for k in range(1, steps + 1):
-        oracle.step(oracle.HParams(optim=wl.optim, step=k, **hp_kw), t, g, wl.dtype, wl.blocksize,
-                    q1, q2)
+        oracle.step(oracle.HParams(optim=wl.optim, step=k, **hp_kw), t, g, wl.dtype,
+                    _oracle_b(wl, t.p.size), q1, q2)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -565,20 +583,22 @@ def time_oracle(wl, n_sample, steps, budget_s):
 
 
 def calibrate_oracle(wl):
-    n, done, el = time_oracle(wl, 16 * wl.blocksize, 2, 10.0)
+    n, done, el = time_oracle(wl, 16 * _gran(wl), 2, 10.0)
     return el / done / n  # seconds per element
 
 
 def cpu_baseline(wl, params=None, budget_s=15.0):
     sec_per_elem = calibrate_oracle(wl)
-    n_sample = int(max(wl.blocksize, min(wl.sizes[0], budget_s / 3 / sec_per_elem)))
-    n_sample -= n_sample % wl.blocksize or 0
-    n_sample = max(wl.blocksize, n_sample)
+    G = _gran(wl)
+    n_sample = int(max(G, min(wl.sizes[0], budget_s / 3 / sec_per_elem)))
+    n_sample -= n_sample % G or 0
+    n_sample = max(G, n_sample)
     n, done, el = time_oracle(wl, n_sample, 3, budget_s)
     value = n * done / el / 1e9
     return {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n:,} of the workload's {wl.elements:,} elements (first tensor, "
-                      f"{n // wl.blocksize:,} blocks), {done} step(s), single-threaded C oracle, "
+                      f"{'tensor-wise' if not wl.blocksize else f'{n // wl.blocksize:,} blocks'}), "
+                      f"{done} step(s), single-threaded C oracle, "
                       f"{el:.1f} s"}
 
 
@@ -590,22 +610,24 @@ def run_reference(args, wl):
     total_budget = args.ref_budget
     sec_per_elem = calibrate_oracle(wl)
     per_step = total_budget / max(1, args.steps + args.warmup)
-    n_sample = int(max(wl.blocksize, min(wl.sizes[0], per_step / sec_per_elem)))
-    n_sample = max(wl.blocksize, n_sample - n_sample % wl.blocksize)
+    G = _gran(wl)
+    n_sample = int(max(G, min(wl.sizes[0], per_step / sec_per_elem)))
+    n_sample = max(G, n_sample - n_sample % G)
     import oracle
     t, g, q1, q2 = _oracle_sample(wl, n_sample)
     for k in range(1, args.warmup + 1):
         oracle.step(oracle.HParams(optim=wl.optim, step=k, **wl.hp), t, g, wl.dtype,
-                    wl.blocksize, q1, q2)
+                    _oracle_b(wl, t.p.size), q1, q2)
     t0 = time.perf_counter()
     for k in range(args.warmup + 1, args.warmup + args.steps + 1):
         oracle.step(oracle.HParams(optim=wl.optim, step=k, **wl.hp), t, g, wl.dtype,
-                    wl.blocksize, q1, q2)
+                    _oracle_b(wl, t.p.size), q1, q2)
     el = time.perf_counter() - t0
     n = t.p.size
     value = n * args.steps / el / 1e9
     sample = (f"{n:,} of the workload's {wl.elements:,} elements per step "
-              f"({n // wl.blocksize:,} blocks of the first tensor), single-threaded C oracle")
+              f"({n // _gran(wl):,} blocks of {_gran(wl)} of the first tensor"
+              f"{', tensor-wise' if not wl.blocksize else ''}), single-threaded C oracle")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,

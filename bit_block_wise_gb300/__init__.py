@@ -234,7 +234,7 @@ def bnb8_workspace_size(params: Sequence[ParamState], hp: HParams) -> int:
 
 def _workspace(params, hp, workspace):
     torch = _torch()
-    if hp.max_unorm == 0.0:
+    if hp.max_unorm == 0.0 and hp.blocksize != 0:
         return None, 0  # the step entry points need no workspace then
     need = bnb8_workspace_size(params, hp)
     if need == 0:
@@ -350,7 +350,9 @@ def split_blocks(ps: ParamState, blocksize: int, nchunks: int):
     cannot split, so it is returned whole.  Returns (element ranges, pieces).
     """
     n = ps.p.numel()
-    if ps.s1.numel() == 2 * n:          # AdEMAMix: m1 and m2 stacked, 8- or 32-bit
+    if ps.s1.numel() == 2 * n or blocksize == 0:
+        # AdEMAMix keeps m1 and m2 stacked (8- or 32-bit); a tensor-wise
+        # tensor is one block
         return [(0, n)], [ps]
     nb = (n + blocksize - 1) // blocksize
     per = max(1, -(-nb // max(1, nchunks)))
@@ -372,7 +374,8 @@ def split_blocks(ps: ParamState, blocksize: int, nchunks: int):
 
 def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256):
     """Allocate the all-zero optimizer state of parameter p (codes of 0.0 in
-    the signed / unsigned maps of bnb8_create_qmap, absmax 0)."""
+    the signed / unsigned maps of bnb8_create_qmap, absmax 0).  blocksize 0:
+    tensor-wise quantization, one absmax per state."""
     torch = _torch()
     n, dev = p.numel(), p.device
     k = NSTATES[optim]
@@ -380,7 +383,7 @@ def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256):
         s1 = torch.zeros(n * (2 if optim == "ademamix" else 1), dtype=torch.float32, device=dev)
         s2 = torch.zeros(n, dtype=torch.float32, device=dev) if k >= 2 else None
         return s1, s2, None, None
-    nb = (n + blocksize - 1) // blocksize
+    nb = 1 if blocksize == 0 else (n + blocksize - 1) // blocksize  # 0: tensor-wise
     signed1 = optim not in ("rmsprop", "adagrad")
     s1 = torch.full((n * (2 if optim == "ademamix" else 1),), 127 if signed1 else 0,
                     dtype=torch.uint8, device=dev)

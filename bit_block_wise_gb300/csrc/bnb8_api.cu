@@ -132,8 +132,14 @@ int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int*
   for (int i = 0; i < nallowed; ++i) ok = ok || hp->optim == allowed[i];
   if (!ok) return fail(BNB8_EINVAL, "optimizer %d not handled by this entry point", hp->optim);
   if (!valid_dtype(hp->dtype)) return fail(BNB8_EINVAL, "unknown dtype %d", hp->dtype);
-  *log2B = log2_blocksize(hp->blocksize);
-  if (*log2B < 0) return fail(BNB8_EINVAL, "blocksize %d is not a power of two in [64, 4096]", hp->blocksize);
+  // blocksize 0: tensor-wise quantization (one absmax per state per tensor);
+  // the kernels then cut each tensor into groups of 256 elements for work
+  *log2B = hp->blocksize == 0 ? 8 : log2_blocksize(hp->blocksize);
+  if (*log2B < 0)
+    return fail(BNB8_EINVAL, "blocksize %d is neither 0 nor a power of two in [64, 4096]",
+                hp->blocksize);
+  if (hp->blocksize == 0 && (hp->flags & BNB8_UNORM_PER_BLOCK) != 0)
+    return fail(BNB8_EINVAL, "BNB8_UNORM_PER_BLOCK needs blocks (blocksize 0 is tensor-wise)");
   if ((hp->flags & ~BNB8_UNORM_PER_BLOCK) != 0)
     return fail(BNB8_EINVAL, "hparams.flags: unknown bits 0x%x", hp->flags & ~BNB8_UNORM_PER_BLOCK);
   if (hp->step < 1) return fail(BNB8_EINVAL, "step must be >= 1 (got %lld)", (long long)hp->step);
@@ -246,10 +252,14 @@ int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace layout: [per-tensor max_unorm multipliers][per-block partials]
+// when the per-tensor pre-pass runs, then [4 words per tensor] of tensor-wise
+// absmax accumulators when blocksize is 0.
 size_t workspace_bytes_for(int nt, int64_t all_blocks) {
   return align256(static_cast<size_t>(nt) * sizeof(float)) +
          align256(static_cast<size_t>(all_blocks) * sizeof(float2));
 }
+size_t tw_bytes_for(int nt) { return align256(static_cast<size_t>(nt) * 4 * sizeof(uint32_t)); }
 
 StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan,
                    const bnb8_hparams& hp, const Scalars& sc, int log2B, const float* qmap1,
@@ -272,6 +282,7 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
   a.max_unorm = hp.max_unorm;
   a.unorm_c = static_cast<float>(sc.unorm_c);
   a.skip_zeros = hp.skip_zeros != 0;
+  a.tensorwise = hp.blocksize == 0 ? 1 : 0;
   a.log2B = log2B;
   a.ntensors = static_cast<int32_t>(c.idx.size());
   a.total_blocks = c.total_blocks;
@@ -304,7 +315,7 @@ cudaError_t launch_family(int bits, int optim, int dtype, int mode, const StepAr
 }
 
 int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int log2B) {
-  static int cache[2][7][3][3] = {};
+  static int cache[2][7][3][5] = {};
   int& c = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
   if (c == 0) {
     if (optim == BNB8_ADAM || optim == BNB8_ADAMW) c = ctas_step_adam(bits, optim, dtype, mode);
@@ -369,23 +380,54 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
   // per-block max_unorm: the norms are formed inside the step itself
   const bool per_block = hp->max_unorm > 0.0f && (hp->flags & BNB8_UNORM_PER_BLOCK) != 0;
   const int mode = per_block ? MODE_BCLIP : MODE_STEP;
-  if (hp->max_unorm > 0.0f && !per_block) {
-    const size_t need = workspace_bytes_for(nt, plan.all_blocks);
-    if (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)
-      return fail(BNB8_EWORKSPACE, "max_unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
-                  need, ws_bytes);
+  const bool prepass = hp->max_unorm > 0.0f && !per_block;
+  const bool tw = hp->blocksize == 0;
+  const size_t need = (prepass ? workspace_bytes_for(nt, plan.all_blocks) : 0) + (tw ? tw_bytes_for(nt) : 0);
+  if (need > 0 && (ws == nullptr || !aligned(ws, 256) || ws_bytes < need))
+    return fail(BNB8_EWORKSPACE, "%s needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+                prepass ? "max_unorm" : "tensor-wise quantization", need, ws_bytes);
+  uint32_t* tw_acc = tw ? reinterpret_cast<uint32_t*>(
+                              static_cast<char*>(ws) + (prepass ? workspace_bytes_for(nt, plan.all_blocks) : 0))
+                        : nullptr;
+  if (prepass) {
     float* scales = static_cast<float*>(ws);
     float2* partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(nt * sizeof(float)));
     rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream);
     if (rc != BNB8_OK) return rc;
     clip = scales;
   }
+  if (tw) {
+    // tensor-wise: the new absmax of every state of every 8-bit tensor first
+    cudaError_t e = launch_fill(reinterpret_cast<float*>(tw_acc), 4 * nt, 0.0f, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-wise fill");
+    for (const Plan::Chunk& c : plan.chunks) {
+      if (c.bits != 8) continue;
+      StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
+      a.clip = clip;
+      a.tw_acc = tw_acc;
+      const int grid = grid_for(8, hp->optim, hp->dtype, MODE_TWMAX, c.total_blocks, log2B);
+      e = launch_family(8, hp->optim, hp->dtype, MODE_TWMAX, a, grid, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor-wise max launch");
+    }
+  }
   for (const Plan::Chunk& c : plan.chunks) {
     StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
     a.clip = clip;
-    const int grid = grid_for(c.bits, hp->optim, hp->dtype, mode, c.total_blocks, log2B);
-    const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, mode, a, grid, stream);
+    a.tw_acc = tw_acc;
+    const int m = (tw && c.bits == 8) ? MODE_TWSTEP : mode;
+    const int grid = grid_for(c.bits, hp->optim, hp->dtype, m, c.total_blocks, log2B);
+    const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, m, a, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "step launch");
+  }
+  if (tw) {
+    // the new absmax is stored once every CTA has dequantized with the old
+    for (const Plan::Chunk& c : plan.chunks) {
+      if (c.bits != 8) continue;
+      StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
+      a.tw_acc = tw_acc;
+      const cudaError_t e = launch_tw_store(hp->optim, a, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor-wise store launch");
+    }
   }
   return BNB8_OK;
 }
@@ -488,7 +530,9 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
                             BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX};
   int log2B = 0;
   if (check_hparams(hp, all, 7, &log2B) != BNB8_OK) return 0;
-  if (hp->max_unorm <= 0.0f || (hp->flags & BNB8_UNORM_PER_BLOCK) != 0) return 0;
+  const bool prepass = hp->max_unorm > 0.0f && (hp->flags & BNB8_UNORM_PER_BLOCK) == 0;
+  const bool tw = hp->blocksize == 0;
+  if (!prepass && !tw) return 0;
   if (ntensors < 0 || (ntensors > 0 && tensors == nullptr)) {
     fail(BNB8_EINVAL, "bad tensor list");
     return 0;
@@ -501,7 +545,7 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
     }
     blocks += (tensors[i].n + (int64_t(1) << log2B) - 1) >> log2B;
   }
-  return workspace_bytes_for(ntensors, blocks);
+  return (prepass ? workspace_bytes_for(ntensors, blocks) : 0) + (tw ? tw_bytes_for(ntensors) : 0);
 }
 
 int bnb8_step_2state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,

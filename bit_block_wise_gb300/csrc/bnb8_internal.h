@@ -15,8 +15,11 @@ constexpr int kTblZero = 2946;      // entry of the smallest positive bucket
 enum Optim { ADAM = 0, ADAMW = 1, MOMENTUM = 2, RMSPROP = 3, ADAGRAD = 4, LION = 5, ADEMAMIX = 6 };
 enum Dtype { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 // MODE_STEP: the update; MODE_NORM: the per-tensor max_unorm pre-pass;
-// MODE_BCLIP: the update with max_unorm applied per block (no pre-pass).
-enum Mode { MODE_STEP = 0, MODE_NORM = 1, MODE_BCLIP = 2 };
+// MODE_BCLIP: the update with max_unorm applied per block (no pre-pass);
+// MODE_TWMAX: tensor-wise quantization's first pass, the new absmax of each
+// state of each tensor (the update is computed, nothing is stored);
+// MODE_TWSTEP: tensor-wise quantization's step (requantized with that absmax).
+enum Mode { MODE_STEP = 0, MODE_NORM = 1, MODE_BCLIP = 2, MODE_TWMAX = 3, MODE_TWSTEP = 4 };
 
 // One tensor of a launch.  Pointers are device pointers.
 struct DevTensor {
@@ -45,6 +48,12 @@ struct StepArgs {
   const float* qmap2;
   const float* clip;     // per-tensor step multipliers (by DevTensor::index) or nullptr
   float2* partials;      // MODE_NORM: per-block (sum u^2, sum p^2), indexed by launch block
+  // Tensor-wise quantization (one absmax per state per tensor): absmax
+  // arrays hold one value per state; tw_acc[4 * index + k] is the new absmax
+  // bit pattern of state k (max-reduced by MODE_TWMAX) and [4 * index + 3]
+  // is nonzero if any element of the tensor is updated.
+  int32_t tensorwise;
+  uint32_t* tw_acc;
   DevTensor t[kMaxTensors];
 };
 
@@ -97,6 +106,9 @@ cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_
 cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);  // both levels
 cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s);
+// Tensor-wise quantization's last step: the new absmax of every tensor of a
+// launch from tw_acc into its absmax arrays (tensors with an update only).
+cudaError_t launch_tw_store(int optim, const StepArgs& a, cudaStream_t s);
 
 // Resident CTAs per SM of a step kernel (sizes the persistent grids).
 int ctas_step_adam(int bits, int optim, int dtype, int mode);

@@ -100,12 +100,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
 
 template <int OPT, int DT, int MODE>
 cudaError_t launch_step32_t(const StepArgs& a, int grid, cudaStream_t s) {
-  k_step32<OPT, DT, MODE><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if constexpr (MODE == MODE_TWMAX || MODE == MODE_TWSTEP) {
+    return cudaErrorInvalidValue;  // 32-bit states have no absmax
+  } else {
+    k_step32<OPT, DT, MODE><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
 }
 
 template <int OPT, int DT, int MODE>
 int ctas_step32_t() {
+  if constexpr (MODE == MODE_TWMAX || MODE == MODE_TWSTEP) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_step32<OPT, DT, MODE>, kThreads, 0) !=
       cudaSuccess)

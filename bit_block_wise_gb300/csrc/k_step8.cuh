@@ -50,7 +50,7 @@ struct Step8Smem {
   static constexpr int kQ = 0;                                   // float q[NM][256]
   static constexpr int kMid = kQ + NM * 256 * 4;                 // float mid[NM][256]
   static constexpr int kTbl = kMid + NM * 256 * 4;               // uint32 tbl[NM][kTblSize]
-  static constexpr int kRed = kTbl + (MODE != MODE_NORM ? NM * kTblSize * 4 : 0);
+  static constexpr int kRed = kTbl + ((MODE == MODE_STEP || MODE == MODE_BCLIP || MODE == MODE_TWSTEP) ? NM * kTblSize * 4 : 0);
   static constexpr int kBytes = kRed + 2 * (kThreads / 32) * 4 * 4;
 };
 
@@ -65,8 +65,10 @@ __device__ __forceinline__ void requantize_store(const float (&s)[Traits<OPT>::N
                                                  int64_t blk, int valid, bool vec, int gtid,
                                                  const bool (&fast_map)[2],
                                                  const bool (&nonneg_map)[2],
-                                                 const uint32_t* stbl, const float* smid) {
+                                                 const uint32_t* stbl, const float* smid,
+                                                 bool store_absmax = true) {
   constexpr int NS = Traits<OPT>::NS;
+  if (!store_absmax) gtid = 1;  // tensor-wise: the absmax is stored after the pass
   float inv[NS];
   bool all_fast = true;
 #pragma unroll
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   uint32_t* stbl = reinterpret_cast<uint32_t*>(smem + L::kTbl);
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
   __shared__ int s_bad[2];
+  __shared__ uint32_t s_tw[4];  // MODE_TWMAX: this CTA's new absmax bits per state, any-update
   __shared__ int s_below[2];
   __shared__ int s_scan[2 * 32];
 
@@ -145,13 +148,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   // ---- stage the maps, midpoints and (step mode) the bucket tables ----
   for (int i = tid; i < NM * 256; i += kThreads) sq[i] = i < 256 ? a.qmap1[i] : a.qmap2[i - 256];
   if (tid < 2) s_bad[tid] = 0;
+  if (tid < 4) s_tw[tid] = 0u;
   __syncthreads();
   for (int i = tid; i < NM * 256; i += kThreads) {
     const int m = i >> 8, k = i & 255;
     smid[i] = k < 255 ? (sq[m * 256 + k] + sq[m * 256 + k + 1]) * 0.5f : 0.0f;
   }
   __syncthreads();
-  if (MODE != MODE_NORM) {
+  if (MODE == MODE_STEP || MODE == MODE_BCLIP || MODE == MODE_TWSTEP) {
     build_tables<NM>(smid, stbl, s_bad, s_below, s_scan);
   }
   const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
@@ -189,9 +193,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     const int64_t n = d.n;
     const int32_t nb = static_cast<int32_t>((n + B - 1) >> log2B);
     const int32_t end = fb + nb;
-    const StatePtrs<OPT> sp = state_ptrs<OPT>(d, nb);
+    // tensor-wise: one absmax per state (index 0; AdEMAMix's absmax1 is
+    // [2, 1]); a tensor none of whose elements is updated (skip_zeros) is
+    // left untouched
+    const bool tw = MODE == MODE_TWMAX || MODE == MODE_TWSTEP ||
+                    (MODE == MODE_NORM && a.tensorwise != 0);
+    const StatePtrs<OPT> sp = state_ptrs<OPT>(d, tw ? 1 : nb);
     const bool vec = d.vec_ok != 0;
     const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
+    if (MODE == MODE_TWSTEP && a.tw_acc[4 * d.index + 3] == 0u) continue;
     // first warp base whose groups can reach this tensor
     const int32_t lo = fb - (groups_per_warp - 1);
     int32_t base = warp_g0;
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       float p[8], g[8];
       uint2 cw[NS];
       float am[NS];
-      if (MODE != MODE_NORM && SKIP) {
+      if ((MODE == MODE_STEP || MODE == MODE_BCLIP || MODE == MODE_TWSTEP) && SKIP) {
         // skip_zeros: read g first; a block whose gradient is all zero is left
         // untouched, so its p, codes and absmax are never read.  Groups of
         // fewer than 32 threads skip only when their whole warp may.
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
           parity ^= 1;
           group_nz = v[0] != 0u;
         }
-        if (!group_nz) continue;
+        if (!group_nz && !tw) continue;
         load8<DT, false>(d.p, e0, valid, vec, p);
       } else {
         load8<DT, false>(d.p, e0, valid, vec, p);
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         cw[k] = kAheadCodes && have_n ? cwn[k] : load_codes(sp.c[k], e0, valid, vec);
-        am[k] = kAheadAm && have_n ? amn[k] : (active ? sp.a[k][blk] : 0.0f);
+        am[k] = kAheadAm && have_n ? amn[k] : (active ? sp.a[k][tw ? 0 : blk] : 0.0f);
       }
 
       // ---- dequantize, update; new states in s, running max of |s| in mx ----
@@ -349,6 +359,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         if (active && gtid == 0) a.partials[fb + blk] = make_float2(r[0], r[1]);
         continue;
       }
+      if constexpr (MODE == MODE_TWMAX) {
+        // the tensor's new absmax: warp maxima into this CTA's shared
+        // accumulators (flushed to tw_acc once per tensor below)
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          const uint32_t w = __reduce_max_sync(0xffffffffu, mx[k]);
+          if (lane == 0 && w != 0u) atomicMax(&s_tw[k], w);
+        }
+        if (__any_sync(0xffffffffu, any && active) && lane == 0) atomicOr(&s_tw[3], 1u);
+        continue;
+      }
       if constexpr (MODE == MODE_BCLIP) {
         // max_unorm per block: U = unorm_c * ||u||, P = ||p|| over the block
         // (group sums as in the pre-pass); clip the step if U > max_unorm * P
@@ -379,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
               if (kAheadCodes) cwn[k] = load_codes(sp.c[k], e0n, 8, true);
-              amn[k] = sp.a[k][blk_n];
+              amn[k] = sp.a[k][tw ? 0 : blk_n];
             }
             have_n = true;
           }
@@ -387,8 +408,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       }
 
       // ---- new absmax per state (bit patterns of non-negative values) ----
-      group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
-      parity ^= 1;
+      if (tw) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) mx[k] = a.tw_acc[4 * d.index + k];
+      } else {
+        group_max_bits<NS>(mx, GT, glocal, reinterpret_cast<uint32_t*>(sred), parity);
+        parity ^= 1;
+      }
       if (SKIP) {
         // whether any element of the group was updated
         bool group_any;
@@ -403,13 +429,46 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         } else {
           group_any = (__ballot_sync(0xffffffffu, any) & gmask) != 0u;
         }
-        if (!group_any) continue;  // nothing updated: codes and absmax untouched
+        if (!group_any && !tw) continue;  // nothing updated: codes and absmax untouched
       }
       // inactive lanes compute along (valid 0) and store nothing
       requantize_store<OPT>(s, mx, sp, e0, blk, active ? valid : 0, vec, active ? gtid : 1,
-                            fast_map, nonneg_map, stbl, smid);
+                            fast_map, nonneg_map, stbl, smid, !tw);
+    }
+    if constexpr (MODE == MODE_TWMAX) {
+      // this CTA's share of the tensor's new absmax, once per tensor
+      __syncthreads();
+      if (tid < NS) {
+        if (s_tw[tid] != 0u) atomicMax(&a.tw_acc[4 * d.index + tid], s_tw[tid]);
+        s_tw[tid] = 0u;
+      } else if (tid == 3) {
+        if (s_tw[3] != 0u) atomicOr(&a.tw_acc[4 * d.index + 3], 1u);
+        s_tw[3] = 0u;
+      }
+      __syncthreads();
     }
   }
+}
+
+// Tensor-wise quantization: after the step, the new absmax of each updated
+// tensor of the launch (one thread per tensor).
+template <int OPT>
+__global__ void k_tw_store(const __grid_constant__ StepArgs a) {
+  constexpr int NS = Traits<OPT>::NS;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= a.ntensors) return;
+  const DevTensor& d = a.t[t];
+  const uint32_t* acc = a.tw_acc + 4 * d.index;
+  if (acc[3] == 0u) return;
+  const StatePtrs<OPT> sp = state_ptrs<OPT>(d, 1);
+#pragma unroll
+  for (int k = 0; k < NS; ++k) sp.a[k][0] = __uint_as_float(acc[k]);
+}
+
+template <int OPT>
+cudaError_t launch_tw_store_t(const StepArgs& a, cudaStream_t s) {
+  k_tw_store<OPT><<<(a.ntensors + 127) / 128, 128, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <int OPT, int DT, int MODE, bool SKIP>

@@ -13,12 +13,18 @@ cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_NORM, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_BCLIP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_TWMAX, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_TWSTEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_NORM, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_BCLIP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_TWMAX, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_TWSTEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_STEP, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_NORM, launch_step8_t, launch_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_BCLIP, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_TWMAX, launch_step8_t, launch_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_TWSTEP, launch_step8_t, launch_step32_t)
   return cudaErrorInvalidValue;
 }
 
@@ -31,12 +37,18 @@ int ctas_step_ademamix(int bits, int optim, int dtype, int mode) {
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_NORM, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_TWMAX, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F32, MODE_TWSTEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_NORM, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_TWMAX, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_BF16, MODE_TWSTEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_STEP, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_NORM, ctas_step8_t, ctas_step32_t)
   BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_BCLIP, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_TWMAX, ctas_step8_t, ctas_step32_t)
+  BNB8_DISPATCH(ADEMAMIX, DT_F16, MODE_TWSTEP, ctas_step8_t, ctas_step32_t)
   return 1;
 }
 

@@ -36,7 +36,8 @@
  *     (IEEE binary16).  All arithmetic is binary32; a value is rounded to its
  *     storage dtype once, to nearest even.
  *   - Block sizes: a power of two from 64 to 4096.  The last block of a
- *     tensor may be partial.
+ *     tensor may be partial.  The step functions also take blocksize 0:
+ *     tensor-wise quantization, one absmax per state per tensor.
  */
 #ifndef BNB8_H
 #define BNB8_H
@@ -107,7 +108,13 @@ typedef struct bnb8_tensor {
 /* Hyperparameters of one update, shared by every tensor of a call.
  *   optim       enum bnb8_optim; must match the entry point.
  *   dtype       enum bnb8_dtype of p and g.
- *   blocksize   B, a power of two in [64, 4096].
+ *   blocksize   B, a power of two in [64, 4096]; or 0: tensor-wise 8-bit
+ *               states ("8-bit Optimizers via Block-wise Quantization"
+ *               compares block-wise against this), one absmax per state per
+ *               tensor (absmax1/absmax2 hold 1 value; AdEMAMix absmax1 = [2]).
+ *               A first pass finds each tensor's new absmax, the step then
+ *               requantizes with it; needs a workspace (bnb8_workspace_size);
+ *               BNB8_UNORM_PER_BLOCK is BNB8_EINVAL with it.
  *   skip_zeros  nonzero: where the raw gradient is exactly 0 the parameter
  *               and its states keep their values; a block whose gradient is
  *               all zero keeps its codes and absmax bit-identical.
@@ -178,7 +185,9 @@ int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const f
                               struct CUstream_st* stream);
 
 /* Bytes of workspace the step functions and bnb8_unorm need for this tensor
- * list (0 when hp->max_unorm == 0 or hp->flags has BNB8_UNORM_PER_BLOCK).  Returns 0 and
+ * list: the per-tensor max_unorm pre-pass's partials (hp->max_unorm > 0
+ * without BNB8_UNORM_PER_BLOCK) plus 16 bytes per tensor for tensor-wise
+ * quantization (hp->blocksize 0); 0 when neither applies.  Returns 0 and
  * sets the error message on invalid arguments. */
 size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp);
 

@@ -55,7 +55,8 @@ def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False
              gscale=1.0, max_unorm=0.0, zero_frac=0.0, seed=0, init="random", extra_hp=None,
              offsets=None):
     """Run `steps` updates of a tensor list on the GPU and on the oracle and
-    compare after every step."""
+    compare after every step.  B = 0: tensor-wise quantization (the oracle
+    takes each tensor as one block)."""
     q1, q2 = map_pair(optim, S, U)
     qd1 = qdev[0] if q1 is S else qdev[1]
     qd2 = None if q2 is None else qdev[1]
@@ -63,10 +64,11 @@ def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False
     for i, n in enumerate(sizes):
         p = _host_to(workloads.normal(n, 0.1, seed + 10 * i), dtype)
         b = bits[i] if isinstance(bits, (list, tuple)) else bits
+        Bo = B or n
         if init == "zero":
-            st = oracle.zero_state(optim, n, b, B, q1, q2)
+            st = oracle.zero_state(optim, n, b, Bo, q1, q2)
         else:
-            st = random_state(optim, n, b, B, seed + 10 * i + 1, q1, q2)
+            st = random_state(optim, n, b, Bo, seed + 10 * i + 1, q1, q2)
         refs.append(oracle.TensorState(p.copy(), *[None if a is None else a.copy() for a in st], b))
         dev = [to_dev(p, dtype)] + [to_dev(a) for a in st]
         if offsets is not None and offsets[i]:
@@ -95,9 +97,10 @@ def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False
                 rng = np.random.default_rng(seed + 7 * k + i)
                 g[rng.random(n) < zero_frac] = 0.0
                 # whole zero blocks too
-                nb = (n + B - 1) // B
+                Bz = B or 256
+                nb = (n + Bz - 1) // Bz
                 for blk in rng.choice(nb, size=max(1, nb // 3), replace=False):
-                    g[blk * B:(blk + 1) * B] = 0.0
+                    g[blk * Bz:(blk + 1) * Bz] = 0.0
             g = _host_to(g, dtype)
             ghost.append(g)
             gd = to_dev(g, dtype)
@@ -111,7 +114,7 @@ def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False
         ohp = oracle.HParams(optim=optim, **hp)
         before = [oracle.to_f32(r.p, dtype).astype(np.float64) for r in refs]
         for i, n in enumerate(sizes):
-            oracle.step(ohp, refs[i], ghost[i], dtype, B, q1, q2)
+            oracle.step(ohp, refs[i], ghost[i], dtype, B or n, q1, q2)
         torch.cuda.synchronize()
         for i, (ps, r) in enumerate(zip(params, refs)):
             tag = f"{optim}/{dtype}/bits{r.state_bits}/B{B}/step{k}/t{i}(n={sizes[i]})"
@@ -513,3 +516,49 @@ def test_step_max_unorm_per_block_skip_zeros(bnb8, qdev, optim):
     run_case(bnb8, qdev, optim, "bf16", [8, 32], 256, [6 * 256 + 3, 700], steps=3,
              skip_zeros=True, zero_frac=0.2, wd=1e-2, max_unorm=0.5, seed=62,
              extra_hp=dict(unorm_per_block=True))
+
+
+# ---------------------------------------------------------------------------
+# tensor-wise quantization (blocksize 0): one absmax per state per tensor,
+# the oracle taking each tensor as a single block
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_step_tensorwise(bnb8, qdev, optim, dtype):
+    run_case(bnb8, qdev, optim, dtype, 8, 0, [7 * 256 + 77, 300 * 256, 5], steps=3, wd=1e-2,
+             seed=70)
+
+
+@pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
+def test_step_tensorwise_skip_zeros(bnb8, qdev, optim):
+    run_case(bnb8, qdev, optim, "bf16", 8, 0, [20 * 256 + 3, 4000], steps=3, skip_zeros=True,
+             zero_frac=0.3, wd=1e-2, seed=71)
+
+
+def test_step_tensorwise_all_zero_gradient_untouched(bnb8, qdev):
+    # skip_zeros with a gradient that is zero everywhere: codes, absmax and p
+    # keep their bits (the oracle leaves the tensor's one block untouched)
+    n = 5000
+    st = random_state("adam", n, 8, n, 72, S, U)
+    p = workloads.normal(n, 0.1, 73)
+    ps = bnb8.ParamState(to_dev(p), to_dev(np.zeros(n, np.float32)), *[to_dev(a) for a in st], 8)
+    bnb8.step([ps], bnb8.HParams(optim="adam", blocksize=0, skip_zeros=True, step=2), qdev[0],
+              qdev[1])
+    torch.cuda.synchronize()
+    assert_same("p", to_host(ps.p), p)
+    for got, want in zip((ps.s1, ps.s2, ps.absmax1, ps.absmax2), st):
+        assert_same("state", to_host(got), want)
+
+
+def test_step_tensorwise_mixed_bits_and_max_unorm(bnb8, qdev):
+    run_case(bnb8, qdev, "adam", "f32", [8, 32, 8], 0, [4000, 300, 256 * 9], steps=3,
+             max_unorm=0.05, wd=1e-2, seed=74)
+
+
+def test_tensorwise_rejects_per_block_unorm(bnb8, qdev):
+    ps = bnb8.ParamState(torch.zeros(512, device="cuda"), torch.zeros(512, device="cuda"),
+                         *bnb8.zero_state(torch.zeros(512, device="cuda"), "adam", 8, 0), 8)
+    with pytest.raises(bnb8.Bnb8Error, match="tensor-wise"):
+        bnb8.step([ps], bnb8.HParams(optim="adam", blocksize=0, max_unorm=1.0,
+                                     unorm_per_block=True), qdev[0], qdev[1])
