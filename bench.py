@@ -51,12 +51,15 @@ FALLBACK_HBM_GBS = 6800.0
 class Workload:
     """A tensor list, its dtype, optimizer and hyperparameters, and the
     algorithmic bytes one step must move (reads + writes of p, g, the state
-    codes / values and the per-block absmax; the 2 KB of maps are ignored)."""
+    codes / values and the per-block absmax; the 2 KB of maps are ignored).
+    op "quantize" / "dequantize": the stand-alone block-wise conversion of
+    one tensor instead of an optimizer step."""
 
-    def __init__(self, name, desc, optim, dtype, sizes, bits, blocksize, hp, grad, p_std=0.02):
+    def __init__(self, name, desc, optim, dtype, sizes, bits, blocksize, hp, grad, p_std=0.02,
+                 op="step"):
         self.name, self.desc, self.optim, self.dtype = name, desc, optim, dtype
         self.sizes, self.bits, self.blocksize, self.hp = sizes, bits, blocksize, hp
-        self.grad, self.p_std = grad, p_std
+        self.grad, self.p_std, self.op = grad, p_std, op
 
     @property
     def elements(self):
@@ -67,6 +70,10 @@ class Workload:
 
     def algorithmic_bytes(self, live_block_frac=1.0):
         e = 4 if self.dtype == "f32" else 2
+        if self.op != "step":
+            # read x, write codes + absmax (quantize), or the reverse
+            n, nb = self.elements, -(-self.elements // self.blocksize)
+            return int(n * e + n + nb * 4)
         ns, B = self.nstates(), self.blocksize
         total = 0.0
         for n, b in zip(self.sizes, self.bits):
@@ -84,6 +91,16 @@ class Workload:
                 # the per-tensor pre-pass reads g, p, states (per block: inside the step)
                 total += n * 2 * e + (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
         return int(total)
+
+
+def _cfg_codec(op):
+    n = 4096 * 4096
+    what = ("float32 -> uint8 codes + absmax" if op == "quantize"
+            else "uint8 codes + absmax -> float32")
+    return Workload(f"{op}_blockwise_4096x4096_f32_B256",
+                    f"stand-alone block-wise {op} of one 4096x4096 tensor ({what}), block 256, "
+                    f"signed dynamic map, x ~ N(0,1e-3) with 1% N(0,1e-1) outliers",
+                    "adam", "f32", [n], [8], 256, {}, ("outliers", 1e-3, 1e-1, 0.01), op=op)
 
 
 def _cfg_unorm(per_block):
@@ -152,6 +169,8 @@ WORKLOADS = {
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
     "adam_4096_tensorwise": lambda: _cfg_adam_4096(B=0),
+    "quantize_4096": lambda: _cfg_codec("quantize"),
+    "dequantize_4096": lambda: _cfg_codec("dequantize"),
     "adam_4096_unorm": lambda: _cfg_unorm(False),
     "adam_4096_unorm_block": lambda: _cfg_unorm(True),
 }
@@ -310,6 +329,8 @@ def build_state(bnb8, wl, device, seed=0):
 
 
 def run_gpu(args, wl):
+    if wl.op != "step":
+        return run_codec(args, wl)
     import torch
     import bit_block_wise_gb300 as bnb8
     from bit_block_wise_gb300 import build as bnb8_build
@@ -383,8 +404,11 @@ def run_gpu(args, wl):
     n_chunks8 = -(-sum(1 for b in wl.bits if b == 8) // 96)
     n_chunks32 = -(-sum(1 for b in wl.bits if b == 32) // 96)
     launches_per_step = n_chunks8 + n_chunks32
-    if wl.hp.get("max_unorm", 0.0) > 0:
-        launches_per_step += 1 + 2 * (n_chunks8 + n_chunks32)   # fill + pre-pass + finalize
+    if wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block"):
+        # fill + per chunk: pre-pass, chunk sums, finalize
+        launches_per_step += 1 + 3 * (n_chunks8 + n_chunks32)
+    if wl.blocksize == 0:
+        launches_per_step += 1 + 2 * n_chunks8                  # fill + absmax pass + store
 
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no, tdt)
@@ -527,6 +551,153 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
                         "on three streams"}
 
 
+def run_codec(args, wl):
+    """The stand-alone block-wise quantize or dequantize of one tensor, timed
+    like a step (L2 flushed before each, CUDA events on the stream)."""
+    import torch
+    import bit_block_wise_gb300 as bnb8
+    from bit_block_wise_gb300 import build as bnb8_build
+
+    world, rank, local = setup_dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    bnb8_build.build()
+    stream = torch.cuda.current_stream()
+    n, B = wl.elements, wl.blocksize
+    nb = -(-n // B)
+    q = bnb8.bnb8_create_qmap(True).to(device)
+    x = workloads.torch_normal_with_outliers(n, wl.grad[1], wl.grad[2], wl.grad[3], 11 + rank,
+                                             device, torch.float32)
+    codes = torch.empty(n, dtype=torch.uint8, device=device)
+    absmax = torch.empty(nb, dtype=torch.float32, device=device)
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    bnb8.bnb8_quantize_blockwise(x, q, B, codes, absmax, stream=stream)
+    quant = wl.op == "quantize"
+
+    def one_step():
+        if quant:
+            bnb8.bnb8_quantize_blockwise(x, q, B, codes, absmax, stream=stream)
+        else:
+            bnb8.bnb8_dequantize_blockwise(codes, absmax, q, B, out=out, stream=stream)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    flush_sink = torch.empty((), dtype=torch.int32, device=device)
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        torch.amax(flush_read, 0, out=flush_sink)
+        starts[k].record(stream)
+        one_step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    rows = sampler.stop() if sampler else []
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world,
+                        device) / args.steps
+
+    # end to end: the input from pinned host memory, the output read back
+    steps_e2e = max(3, min(args.steps, 50))
+    if quant:
+        h_in = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        h_in.copy_(x)
+        h_codes = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        h_absmax = torch.empty(nb, dtype=torch.float32, pin_memory=True)
+    else:
+        h_codes = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        h_codes.copy_(codes)
+        h_absmax = torch.empty(nb, dtype=torch.float32, pin_memory=True)
+        h_absmax.copy_(absmax)
+        h_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps_e2e):
+        if quant:
+            x.copy_(h_in, non_blocking=True)
+            one_step()
+            h_codes.copy_(codes, non_blocking=True)
+            h_absmax.copy_(absmax, non_blocking=True)
+        else:
+            codes.copy_(h_codes, non_blocking=True)
+            absmax.copy_(h_absmax, non_blocking=True)
+            one_step()
+            h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / steps_e2e
+    in_b, out_b = (n * 4, n + nb * 4) if quant else (n + nb * 4, n * 4)
+
+    alg = wl.algorithmic_bytes()
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(world * n / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.desc, "name": wl.name, "elements": n, "blocksize": B,
+                   "l2": "flushed before every timed step (256 MiB written, then 256 MiB of "
+                         "other data read, leaving clean unrelated lines)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_step": alg, "traffic": ncu_traffic(wl.name)},
+        "e2e": {"value": round(n / (ms_e2e * 1e-3) / 1e9, 3), "unit": UNIT,
+                "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b,
+                "ms_per_step": round(ms_e2e, 4), "steps": steps_e2e,
+                "pipeline": "upload, convert and read back in stream order"},
+        "gpu_launches": args.steps,
+        "clocks": summarize_clocks(rows, t0, t1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = codec_baseline(wl, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def codec_baseline(wl, budget_s):
+    """The oracle's quantize / dequantize on a bounded leading sample."""
+    import oracle
+    oracle.build()
+    B = wl.blocksize
+    q = oracle.create_qmap(True)
+    n = min(wl.elements, 64 * B)
+    done_n, t0 = 0, time.perf_counter()
+    while True:
+        x = workloads.normal_with_outliers(n, wl.grad[1], wl.grad[2], wl.grad[3], 3)
+        if wl.op == "quantize":
+            t1 = time.perf_counter()
+            oracle.quantize_blockwise(x, "f32", q, B)
+        else:
+            c, a = oracle.quantize_blockwise(x, "f32", q, B)
+            t1 = time.perf_counter()
+            oracle.dequantize_blockwise(c, a, q, B, "f32")
+        el = time.perf_counter() - t1
+        done_n += n
+        if time.perf_counter() - t0 > budget_s / 2 or n >= wl.elements:
+            break
+        n = int(min(wl.elements, max(n, n * min(8.0, budget_s / 4 / max(el, 1e-6)))))
+        n -= n % B
+    value = n / el / 1e9
+    return {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n:,} of the workload's {wl.elements:,} elements, one {wl.op}, "
+                      f"single-threaded C oracle, {el:.2f} s"}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -606,6 +777,18 @@ def run_reference(args, wl):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
+        return
+    if wl.op != "step":
+        base = codec_baseline(wl, args.ref_budget)
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": base["value"],
+                          "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                          "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                          "config": {"workload": wl.desc, "name": wl.name,
+                                     "elements": wl.elements, "blocksize": wl.blocksize},
+                          "cpu_baseline": base,
+                          "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
         return
     total_budget = args.ref_budget
     sec_per_elem = calibrate_oracle(wl)

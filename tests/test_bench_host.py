@@ -124,3 +124,16 @@ def test_e2e_groups_cover_every_element_once(name, unorm):
         assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
         if unorm > 0:
             assert len(ranges) == 1
+
+
+@pytest.mark.parametrize("name", ["quantize_4096", "dequantize_4096"])
+def test_codec_workloads_bytes_and_reference_arm(name, capsys):
+    # the stand-alone conversion: x (4 B) + codes (1 B) + absmax (4 B per block)
+    wl = bench.WORKLOADS[name]()
+    n = 4096 * 4096
+    assert wl.algorithmic_bytes() == n * 4 + n + (n // 256) * 4
+    bench.main(["--impl", "reference", "--workload", name, "--steps", "1", "--warmup", "3",
+                "--ref-budget", "2"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
