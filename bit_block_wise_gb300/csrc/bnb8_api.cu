@@ -438,7 +438,7 @@ extern "C" {
 
 const char* bnb8_last_error(void) { return g_last_error.c_str(); }
 
-int bnb8_version(void) { return 100; }
+int bnb8_version(void) { return 200; }  // 0.2.0: hparams.flags, blocksize 0
 
 // Dynamic map (see include/bnb8.h).  Levels are emitted directly in ascending
 // order: the negative levels from the largest magnitude down, zero, the

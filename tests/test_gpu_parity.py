@@ -562,3 +562,31 @@ def test_tensorwise_rejects_per_block_unorm(bnb8, qdev):
     with pytest.raises(bnb8.Bnb8Error, match="tensor-wise"):
         bnb8.step([ps], bnb8.HParams(optim="adam", blocksize=0, max_unorm=1.0,
                                      unorm_per_block=True), qdev[0], qdev[1])
+
+
+def test_step_tensorwise_list_over_launch_capacity(bnb8, qdev):
+    # more tensors than one launch carries: the absmax accumulators are
+    # indexed by the caller's list position across launches
+    rng = np.random.default_rng(75)
+    sizes = [int(x) for x in rng.integers(1, 3000, 130)]
+    bits = [8 if n >= 1024 else 32 for n in sizes]
+    run_case(bnb8, qdev, "adam", "bf16", bits, 0, sizes, steps=2, seed=76)
+
+
+@pytest.mark.parametrize("blocksize,extra", [(0, {}), (256, dict(max_unorm=0.5, unorm_per_block=True))])
+def test_stepper_with_options(bnb8, qdev, blocksize, extra):
+    # tensor-wise (workspace) and per-block max_unorm through a Stepper
+    n = 256 * 40 + 9
+    st = random_state("adam", n, 8, blocksize or n, 80, S, U)
+    p = workloads.normal(n, 0.1, 81)
+    g = to_dev(workloads.normal(n, 1e-2, 82))
+    a = bnb8.ParamState(to_dev(p), g, *[to_dev(x) for x in st], 8)
+    b = bnb8.ParamState(to_dev(p), g, *[to_dev(x) for x in st], 8)
+    hp = dict(HP_BASE["adam"], weight_decay=1e-2, blocksize=blocksize, **extra)
+    stepper = bnb8.Stepper([b], bnb8.HParams(optim="adam", step=1, **hp), qdev[0], qdev[1])
+    for k in range(1, 4):
+        bnb8.step([a], bnb8.HParams(optim="adam", step=k, **hp), qdev[0], qdev[1])
+        stepper(k)
+    torch.cuda.synchronize()
+    for name in ("p", "s1", "s2", "absmax1", "absmax2"):
+        assert_same(name, to_host(getattr(b, name)), to_host(getattr(a, name)))
