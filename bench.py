@@ -263,10 +263,12 @@ def hbm_peak():
 
 
 def kernel_source_hash():
+    """Hash of the device code (kernel files, device helpers, launch
+    arguments): the host API can change without invalidating a capture."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_block_wise_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.startswith("k_") or name in ("bnb8_device.cuh", "bnb8_internal.h"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
