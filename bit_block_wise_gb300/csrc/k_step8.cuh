@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
           for (int k = 0; k < NS; ++k) {
             s[k][j] = st[k].x;
             s[k][j + 1] = st[k].y;
-            mx[k] = max(mx[k], max(__float_as_uint(fabsf(st[k].x)), __float_as_uint(fabsf(st[k].y))));
+            mx[k] = absmax_nan(mx[k], st[k].x, st[k].y);
           }
         }
         any = true;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
           for (int k = 0; k < NS; ++k) {
             s[k][j] = st[k];
-            mx[k] = max(mx[k], __float_as_uint(fabsf(st[k])));
+            mx[k] = absmax_nan(mx[k], st[k], 0.0f);
           }
         }
         if (!SKIP) any = true;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
 #pragma unroll
           for (int k = 0; k < NS; ++k) {
             s[k][j] = j < valid ? st[k] : 0.0f;
-            mx[k] = max(mx[k], __float_as_uint(fabsf(s[k][j])));
+            mx[k] = absmax_nan(mx[k], s[k][j], 0.0f);
           }
         }
       }
