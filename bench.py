@@ -93,6 +93,27 @@ class Workload:
         return int(total)
 
 
+_HP_1STATE = {"momentum": dict(lr=0.01, beta1=0.9), "rmsprop": dict(lr=0.01, beta1=0.99),
+              "adagrad": dict(lr=0.01), "lion": dict(lr=1e-4, beta1=0.9, beta2=0.99)}
+
+
+def _cfg_embedding(optim, skip):
+    name = {"momentum": "Momentum", "rmsprop": "RMSprop", "adagrad": "Adagrad", "lion": "Lion"}[optim]
+    return Workload(
+        f"{optim}8bit_50257x1024_bf16_B256_rowsparse_{'skipzeros' if skip else 'noskip'}",
+        f"{name}8bit on a 50,257 x 1,024 bf16 embedding, 90% of gradient rows exactly zero, "
+        f"skip_zeros {'on' if skip else 'off'}",
+        optim, "bf16", [50257 * 1024], [8], 256, dict(_HP_1STATE[optim], skip_zeros=skip),
+        ("rows", 50257, 1024, 0.1, 1e-3))
+
+
+def _cfg_dense_1state(optim):
+    name = {"rmsprop": "RMSprop", "adagrad": "Adagrad"}[optim]
+    return Workload(f"{optim}8bit_64M_bf16_B256", f"{name}8bit, 67,108,864 dense bf16",
+                    optim, "bf16", [1 << 26], [8], 256, dict(_HP_1STATE[optim]),
+                    ("normal", 1e-3))
+
+
 def _cfg_codec(op):
     n = 4096 * 4096
     what = ("float32 -> uint8 codes + absmax" if op == "quantize"
@@ -168,7 +189,12 @@ WORKLOADS = {
                                           alpha=5.0, t_alpha=100, t_beta3=100, eps=1e-8),
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
+    **{f"{o}_embedding{sfx}": (lambda o=o, sk=sk: _cfg_embedding(o, sk))
+       for o in ("momentum", "rmsprop", "adagrad", "lion") for sfx, sk in (("", True), ("_noskip", False))
+       if not (o == "momentum" and sk)},
+    **{f"{o}_64m": (lambda o=o: _cfg_dense_1state(o)) for o in ("rmsprop", "adagrad")},
     "adam_4096_tensorwise": lambda: _cfg_adam_4096(B=0),
+    "adamw_4096_b2048": lambda: _cfg_adam_4096("adamw", 2048),
     "quantize_4096": lambda: _cfg_codec("quantize"),
     "dequantize_4096": lambda: _cfg_codec("dequantize"),
     "adam_4096_unorm": lambda: _cfg_unorm(False),
