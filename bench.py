@@ -94,11 +94,13 @@ class Workload:
 
 
 _HP_1STATE = {"momentum": dict(lr=0.01, beta1=0.9), "rmsprop": dict(lr=0.01, beta1=0.99),
-              "adagrad": dict(lr=0.01), "lion": dict(lr=1e-4, beta1=0.9, beta2=0.99)}
+              "adagrad": dict(lr=0.01), "lion": dict(lr=1e-4, beta1=0.9, beta2=0.99),
+              "adam": dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)}
 
 
 def _cfg_embedding(optim, skip):
-    name = {"momentum": "Momentum", "rmsprop": "RMSprop", "adagrad": "Adagrad", "lion": "Lion"}[optim]
+    name = {"momentum": "Momentum", "rmsprop": "RMSprop", "adagrad": "Adagrad", "lion": "Lion",
+            "adam": "Adam"}[optim]
     return Workload(
         f"{optim}8bit_50257x1024_bf16_B256_rowsparse_{'skipzeros' if skip else 'noskip'}",
         f"{name}8bit on a 50,257 x 1,024 bf16 embedding, 90% of gradient rows exactly zero, "
@@ -190,7 +192,7 @@ WORKLOADS = {
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
     **{f"{o}_embedding{sfx}": (lambda o=o, sk=sk: _cfg_embedding(o, sk))
-       for o in ("momentum", "rmsprop", "adagrad", "lion") for sfx, sk in (("", True), ("_noskip", False))
+       for o in ("momentum", "rmsprop", "adagrad", "lion", "adam") for sfx, sk in (("", True), ("_noskip", False))
        if not (o == "momentum" and sk)},
     **{f"{o}_64m": (lambda o=o: _cfg_dense_1state(o)) for o in ("rmsprop", "adagrad")},
     "adam_4096_tensorwise": lambda: _cfg_adam_4096(B=0),

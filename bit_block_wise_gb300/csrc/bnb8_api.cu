@@ -282,6 +282,9 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
   a.max_unorm = hp.max_unorm;
   a.unorm_c = static_cast<float>(sc.unorm_c);
   a.skip_zeros = hp.skip_zeros != 0;
+  a.zero_ratio = sc.eps_hat > 0.0f && std::isfinite(sc.eps_hat) && std::isfinite(sc.b1) &&
+                 std::isfinite(sc.b2) && std::isfinite(sc.omb1) && std::isfinite(sc.omb2) &&
+                 std::isfinite(hp.gnorm_scale);
   a.tensorwise = hp.blocksize == 0 ? 1 : 0;
   a.log2B = log2B;
   a.ntensors = static_cast<int32_t>(c.idx.size());

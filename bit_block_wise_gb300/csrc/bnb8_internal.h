@@ -53,6 +53,10 @@ struct StepArgs {
   // bit pattern of state k (max-reduced by MODE_TWMAX) and [4 * index + 3]
   // is nonzero if any element of the tensor is updated.
   int32_t tensorwise;
+  // 1 if a zero gradient over zero moments has the update direction of its
+  // (signed zero) numerator exactly: eps_hat > 0 and finite, and finite
+  // betas, 1 - betas and gradient scale
+  int32_t zero_ratio;
   uint32_t* tw_acc;
   DevTensor t[kMaxTensors];
 };

@@ -129,6 +129,28 @@ __device__ __forceinline__ void requantize_store(const float (&s)[Traits<OPT>::N
   }
 }
 
+// Eight zero gradients over zero states of RMSprop or Adagrad, on packed
+// pairs (StepArgs::zero_ratio holds): the state and p update as usual, with
+// the update direction the scaled gradient itself, which is the exact value
+// of g / (sqrt(+0) + eps_hat) (pair_dir ZERO).
+template <int OPT>
+__device__ __forceinline__ void zero_rows_update(const StepArgs& a, const float* sq, uint2 cw,
+                                                 float am, float (&p)[8], const float (&g)[8],
+                                                 float eff, float (&s)[8], uint32_t& mx) {
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    float2 st[3] = {mul2(make_float2(sq[code_byte(cw, j)], sq[code_byte(cw, j + 1)]), f2(am)),
+                    f2(0.0f), f2(0.0f)};
+    float2 pp = make_float2(p[j], p[j + 1]);
+    pair_update<OPT, true>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
+    p[j] = pp.x;
+    p[j + 1] = pp.y;
+    s[j] = st[0].x;
+    s[j + 1] = st[0].y;
+    mx = absmax_nan(mx, st[0].x, st[0].y);
+  }
+}
+
 template <int OPT, int DT, int MODE, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ StepArgs a) {
   constexpr int NS = Traits<OPT>::NS;
@@ -150,11 +172,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   if (tid < 2) s_bad[tid] = 0;
   if (tid < 4) s_tw[tid] = 0u;
   __syncthreads();
+  // Rows with a zero gradient over zero states (untouched rows of an
+  // embedding) skip the square root and division of RMSprop and Adagrad,
+  // exactly (pair_dir ZERO).  Adam keeps one path: at its register budget a
+  // second copy of the packed loop costs more on dense gradients than the
+  // zero rows gain.
+  constexpr bool kZeroPath = (OPT == RMSPROP || OPT == ADAGRAD) && MODE == MODE_STEP;
+  static_assert(!kZeroPath || NS == 1, "the zero check reads one state absmax");
+  bool fin = true;
   for (int i = tid; i < NM * 256; i += kThreads) {
     const int m = i >> 8, k = i & 255;
     smid[i] = k < 255 ? (sq[m * 256 + k] + sq[m * 256 + k + 1]) * 0.5f : 0.0f;
+    if (kZeroPath) fin = fin && fabsf(sq[i]) <= FLT_MAX;
   }
-  __syncthreads();
+  // whether every map level is finite (a zero absmax then dequantizes to zeros)
+  bool maps_finite = false;
+  if constexpr (kZeroPath) {
+    maps_finite = __syncthreads_and(fin) != 0;
+  } else {
+    __syncthreads();
+  }
   if (MODE == MODE_STEP || MODE == MODE_BCLIP || MODE == MODE_TWSTEP) {
     build_tables<NM>(smid, stbl, s_bad, s_below, s_scan);
   }
@@ -213,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
     // the other kernels would spill and keep the plain order
     constexpr bool kAheadAm = MODE == MODE_STEP && !SKIP && (NS == 1 || (NS == 2 && DT == DT_F32));
     constexpr bool kAheadCodes = MODE == MODE_STEP && !SKIP && NS == 1;
+    const bool zero_ok = kZeroPath && a.zero_ratio != 0 && maps_finite &&
+                         (Traits<OPT>::DECOUPLED || a.wd == 0.0f);
     bool have_n = false;
     uint2 cwn[NS];
     float amn[NS];
@@ -268,33 +307,45 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       if (!SKIP && __all_sync(0xffffffffu, full)) {
         // every thread of the warp holds 8 present, aligned elements: a
         // straight-line path on packed pairs, no per-element predicates
+        bool zero = false;
+        if constexpr (kZeroPath) {
+          if (zero_ok) {
+            uint32_t o = 0u;
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float2 st[3];
-#pragma unroll
-          for (int k = 0; k < 3; ++k)
-            st[k] = k < NS ? mul2(make_float2(sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)],
-                                              sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j + 1)]),
-                                  f2(am[k]))
-                           : f2(0.0f);
-          if (MODE != MODE_STEP) psq = psq + p[j] * p[j] + p[j + 1] * p[j + 1];
-          float2 pp = make_float2(p[j], p[j + 1]);
-          float2 u;
-          if (MODE == MODE_BCLIP) {
-            u = pair_dir<OPT>(a, pp, make_float2(g[j], g[j + 1]), st);
-            ud[j] = u.x;
-            ud[j + 1] = u.y;
-          } else {
-            u = pair_update<OPT>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
-            p[j] = pp.x;
-            p[j + 1] = pp.y;
+            for (int j = 0; j < 8; ++j) o |= __float_as_uint(g[j]);
+            zero = (o << 1) == 0u && am[0] == 0.0f;  // eight +-0 gradients, zero states
           }
-          if (MODE != MODE_STEP) usq = usq + u.x * u.x + u.y * u.y;
+          if (zero) zero_rows_update<OPT>(a, sq, cw[0], am[0], p, g, eff, s[0], mx[0]);
+        }
+        if (!zero) {
 #pragma unroll
-          for (int k = 0; k < NS; ++k) {
-            s[k][j] = st[k].x;
-            s[k][j + 1] = st[k].y;
-            mx[k] = absmax_nan(mx[k], st[k].x, st[k].y);
+          for (int j = 0; j < 8; j += 2) {
+            float2 st[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+              st[k] = k < NS ? mul2(make_float2(sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j)],
+                                                sq[Traits<OPT>::map_of(k) * 256 + code_byte(cw[k], j + 1)]),
+                                    f2(am[k]))
+                             : f2(0.0f);
+            if (MODE != MODE_STEP) psq = psq + p[j] * p[j] + p[j + 1] * p[j + 1];
+            float2 pp = make_float2(p[j], p[j + 1]);
+            float2 u;
+            if (MODE == MODE_BCLIP) {
+              u = pair_dir<OPT>(a, pp, make_float2(g[j], g[j + 1]), st);
+              ud[j] = u.x;
+              ud[j + 1] = u.y;
+            } else {
+              u = pair_update<OPT>(a, -eff, pp, make_float2(g[j], g[j + 1]), st);
+              p[j] = pp.x;
+              p[j + 1] = pp.y;
+            }
+            if (MODE != MODE_STEP) usq = usq + u.x * u.x + u.y * u.y;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+              s[k][j] = st[k].x;
+              s[k][j + 1] = st[k].y;
+              mx[k] = absmax_nan(mx[k], st[k].x, st[k].y);
+            }
           }
         }
         any = true;

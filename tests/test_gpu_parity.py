@@ -53,7 +53,7 @@ def _host_to(x, dtype):
 
 def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False, wd=0.0,
              gscale=1.0, max_unorm=0.0, zero_frac=0.0, seed=0, init="random", extra_hp=None,
-             offsets=None):
+             offsets=None, neg_zero=False):
     """Run `steps` updates of a tensor list on the GPU and on the oracle and
     compare after every step.  B = 0: tensor-wise quantization (the oracle
     takes each tensor as one block)."""
@@ -101,6 +101,8 @@ def run_case(bnb8, qdev, optim, dtype, bits, B, sizes, steps=3, skip_zeros=False
                 nb = (n + Bz - 1) // Bz
                 for blk in rng.choice(nb, size=max(1, nb // 3), replace=False):
                     g[blk * Bz:(blk + 1) * Bz] = 0.0
+                if neg_zero:
+                    g[(g == 0.0) & (rng.random(n) < 0.5)] = -0.0
             g = _host_to(g, dtype)
             ghost.append(g)
             gd = to_dev(g, dtype)
@@ -250,6 +252,17 @@ def test_step_from_zero_state(bnb8, qdev, optim, dtype):
 def test_step_skip_zeros(bnb8, qdev, optim, bits, B):
     run_case(bnb8, qdev, optim, "bf16", bits, B, [6 * B + 3], steps=3, skip_zeros=True,
              zero_frac=0.2, wd=1e-2, seed=4)
+
+
+@pytest.mark.parametrize("optim", OPTIMS)
+@pytest.mark.parametrize("bits", [8, 32])
+@pytest.mark.parametrize("init", ["zero", "random"])
+def test_step_zero_gradients_not_skipped(bnb8, qdev, optim, bits, init):
+    """Zero gradients (+0 and -0) with skip_zeros off and no decay: from a zero
+    state the second moments stay exactly 0 (sqrt(0) + eps), and zero
+    numerators reach the division (0 / d)."""
+    run_case(bnb8, qdev, optim, "bf16", bits, 256, [6 * 256 + 3, 1000], steps=3, zero_frac=0.3,
+             init=init, seed=44, neg_zero=True)
 
 
 @pytest.mark.parametrize("optim", OPTIMS)
