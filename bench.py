@@ -53,13 +53,17 @@ class Workload:
     algorithmic bytes one step must move (reads + writes of p, g, the state
     codes / values and the per-block absmax; the 2 KB of maps are ignored).
     op "quantize" / "dequantize": the stand-alone block-wise conversion of
-    one tensor instead of an optimizer step."""
+    one tensor instead of an optimizer step.
+    paged "resident": the states live in paged (managed) memory and every step
+    prefetches them to the device first, as the paged optimizers do; "evicted":
+    the same, with the states paged out to the host before every step (outside
+    the timed region), so that each timed step migrates them back."""
 
     def __init__(self, name, desc, optim, dtype, sizes, bits, blocksize, hp, grad, p_std=0.02,
-                 op="step"):
+                 op="step", paged=None):
         self.name, self.desc, self.optim, self.dtype = name, desc, optim, dtype
         self.sizes, self.bits, self.blocksize, self.hp = sizes, bits, blocksize, hp
-        self.grad, self.p_std, self.op = grad, p_std, op
+        self.grad, self.p_std, self.op, self.paged = grad, p_std, op, paged
 
     @property
     def elements(self):
@@ -151,6 +155,19 @@ def _cfg_adam_4096(optim="adam", B=256):
         ("outliers", 1e-3, 1e-1, 0.01))
 
 
+def _cfg_paged(mode):
+    n = 4096 * 4096
+    how = ("resident, prefetched to the device before every step" if mode == "resident" else
+           "paged out to the host before every step, migrated back inside the timed step")
+    return Workload(
+        f"adam8bit_4096x4096_f32_B256_paged_{mode}",
+        f"PagedAdam8bit blockwise, one 4096x4096 float32 tensor, block 256, states in paged "
+        f"(managed) memory {how}, g ~ N(0,1e-3) with 1% N(0,1e-1) outliers, wd 1e-2",
+        "adam", "f32", [n], [8], 256,
+        dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2),
+        ("outliers", 1e-3, 1e-1, 0.01), paged=mode)
+
+
 def _cfg_gpt2xl():
     shapes = workloads.gpt2_xl_params()
     sizes = [n for _, n in shapes]
@@ -196,6 +213,8 @@ WORKLOADS = {
        if not (o == "momentum" and sk)},
     **{f"{o}_64m": (lambda o=o: _cfg_dense_1state(o)) for o in ("rmsprop", "adagrad")},
     "adam_4096_tensorwise": lambda: _cfg_adam_4096(B=0),
+    "adam_4096_paged": lambda: _cfg_paged("resident"),
+    "adam_4096_paged_evicted": lambda: _cfg_paged("evicted"),
     "adamw_4096_b2048": lambda: _cfg_adam_4096("adamw", 2048),
     "quantize_4096": lambda: _cfg_codec("quantize"),
     "dequantize_4096": lambda: _cfg_codec("dequantize"),
@@ -353,7 +372,7 @@ def build_state(bnb8, wl, device, seed=0):
     params = []
     for i, (n, b) in enumerate(zip(wl.sizes, wl.bits)):
         p = workloads.torch_normal(n, wl.p_std, seed + i, device, tdt)
-        s1, s2, a1, a2 = bnb8.zero_state(p, wl.optim, b, wl.blocksize)
+        s1, s2, a1, a2 = bnb8.zero_state(p, wl.optim, b, wl.blocksize, paged=wl.paged is not None)
         params.append(bnb8.ParamState(p, None, s1, s2, a1, a2, b))
     return params, tdt
 
@@ -394,15 +413,25 @@ def run_gpu(args, wl):
         torch.amax(flush_read, 0, out=flush_sink)
 
     step_no = [0]
+    state_arrays = [t for ps in params for t in (ps.s1, ps.s2, ps.absmax1, ps.absmax2)
+                    if t is not None]
+
+    def page_out():
+        # device-memory pressure elsewhere has moved the states to the host
+        if wl.paged == "evicted":
+            bnb8.paged_prefetch(state_arrays, "cpu", stream)
 
     def one_step(k):
         step_no[0] += 1
         for ps, g in zip(params, grads[k % pool]):
             ps.g = g
+        if wl.paged is not None:
+            bnb8.paged_prefetch(state_arrays, device, stream)  # one call per paged buffer
         hp = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=step_no[0], **hp_kw)
         bnb8.step(params, hp, q1, q2, workspace=workspace if ws_bytes else None, stream=stream)
 
     for k in range(args.warmup):
+        page_out()
         one_step(k)
     torch.cuda.synchronize()
 
@@ -420,6 +449,7 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
+        page_out()
         flush_l2()
         starts[k].record(stream)
         one_step(args.warmup + k)
@@ -466,6 +496,11 @@ def run_gpu(args, wl):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": summarize_clocks(rows, t0, t1),
     }
+    if wl.paged:
+        out["config"]["paged"] = {
+            "mode": wl.paged,
+            "state_bytes": int(sum(t.numel() * t.element_size() for t in state_arrays)),
+            "migrated_host_to_device_in_timed_step": wl.paged == "evicted"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, params, budget_s=args.cpu_budget)
     if rank == 0:

@@ -24,6 +24,7 @@ BNB8_OK, BNB8_EINVAL, BNB8_EUNSUPPORTED, BNB8_ECUDA, BNB8_EWORKSPACE = 0, 1, 2, 
 BNB8_F32, BNB8_BF16, BNB8_F16 = 0, 1, 2
 BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX = range(7)
 BNB8_UNORM_PER_BLOCK = 1
+BNB8_PAGED_HOST = -1
 
 OPTIMS = {"adam": BNB8_ADAM, "adamw": BNB8_ADAMW, "momentum": BNB8_MOMENTUM,
           "rmsprop": BNB8_RMSPROP, "adagrad": BNB8_ADAGRAD, "lion": BNB8_LION,
@@ -37,7 +38,8 @@ MIN_8BIT_SIZE = 4096
 # every symbol include/bnb8.h declares
 EXPORTS = ("bnb8_last_error", "bnb8_version", "bnb8_create_qmap", "bnb8_quantize_blockwise",
            "bnb8_dequantize_blockwise", "bnb8_workspace_size", "bnb8_step_2state",
-           "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm", "bnb8_unorm_static")
+           "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm", "bnb8_unorm_static",
+           "bnb8_paged_alloc", "bnb8_paged_prefetch", "bnb8_paged_free")
 
 
 class Bnb8Tensor(ctypes.Structure):
@@ -89,6 +91,9 @@ def lib() -> ctypes.CDLL:
                                  vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.bnb8_unorm_static.argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
                                         ctypes.POINTER(Bnb8Hparams), vp, vp, vp, vp]
+        L.bnb8_paged_alloc.argtypes = [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]
+        L.bnb8_paged_prefetch.argtypes = [vp, ctypes.c_size_t, i32, vp]
+        L.bnb8_paged_free.argtypes = [vp]
         for name in EXPORTS:
             if name not in ("bnb8_last_error", "bnb8_version", "bnb8_workspace_size"):
                 getattr(L, name).restype = i32
@@ -372,24 +377,141 @@ def split_blocks(ps: ParamState, blocksize: int, nchunks: int):
     return ranges, pieces
 
 
-def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256):
+def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256, paged: bool = False):
     """Allocate the all-zero optimizer state of parameter p (codes of 0.0 in
     the signed / unsigned maps of bnb8_create_qmap, absmax 0).  blocksize 0:
-    tensor-wise quantization, one absmax per state."""
+    tensor-wise quantization, one absmax per state.  paged: the state arrays
+    share one paged (managed) buffer (``paged_zero_states``)."""
+    if paged:
+        return paged_zero_states([(p, optim, state_bits, blocksize)])[0]
     torch = _torch()
-    n, dev = p.numel(), p.device
+    out = []
+    for present, spec in _state_arrays(p.numel(), optim, state_bits, blocksize):
+        if present is None:
+            out.append(None)
+            continue
+        count, dtype, value = spec
+        out.append(torch.full((count,), value, dtype=dtype, device=p.device))
+    return tuple(out)
+
+
+def _state_arrays(n: int, optim: str, state_bits: int, blocksize: int):
+    """(s1, s2, absmax1, absmax2) of an n-element parameter as
+    (present, (count, dtype, zero value)) pairs."""
+    torch = _torch()
     k = NSTATES[optim]
+    m = 2 if optim == "ademamix" else 1
     if state_bits == 32:
-        s1 = torch.zeros(n * (2 if optim == "ademamix" else 1), dtype=torch.float32, device=dev)
-        s2 = torch.zeros(n, dtype=torch.float32, device=dev) if k >= 2 else None
-        return s1, s2, None, None
+        return [(1, (n * m, torch.float32, 0.0)), (1 if k >= 2 else None, (n, torch.float32, 0.0)),
+                (None, None), (None, None)]
     nb = 1 if blocksize == 0 else (n + blocksize - 1) // blocksize  # 0: tensor-wise
-    signed1 = optim not in ("rmsprop", "adagrad")
-    s1 = torch.full((n * (2 if optim == "ademamix" else 1),), 127 if signed1 else 0,
-                    dtype=torch.uint8, device=dev)
-    a1 = torch.zeros(nb * (2 if optim == "ademamix" else 1), dtype=torch.float32, device=dev)
-    s2 = a2 = None
-    if k >= 2:
-        s2 = torch.zeros(n, dtype=torch.uint8, device=dev)
-        a2 = torch.zeros(nb, dtype=torch.float32, device=dev)
-    return s1, s2, a1, a2
+    zero1 = 127 if optim not in ("rmsprop", "adagrad") else 0  # code of 0.0 in the map of s1
+    two = 1 if k >= 2 else None
+    return [(1, (n * m, torch.uint8, zero1)), (two, (n, torch.uint8, 0)),
+            (1, (nb * m, torch.float32, 0.0)), (two, (nb, torch.float32, 0.0))]
+
+
+# ---- paged state -----------------------------------------------------------------
+
+class _PagedBuffer:
+    """One bnb8_paged_alloc buffer, exposed through the CUDA array interface:
+    torch.as_tensor wraps it without a copy and holds a reference to this
+    object for the tensor's lifetime; the buffer is freed with the last
+    reference."""
+
+    def __init__(self, count: int, dtype):
+        torch = _torch()
+        esize = torch.empty((), dtype=dtype).element_size()
+        typestr = {torch.uint8: "|u1", torch.float32: "<f4", torch.float16: "<f2"}.get(dtype)
+        if typestr is None:
+            raise ValueError(f"paged buffers hold uint8, float32 or float16, not {dtype}")
+        self.ptr = None
+        ptr = ctypes.c_void_p()
+        _check(lib().bnb8_paged_alloc(max(count * esize, 1), ctypes.byref(ptr)))
+        self.ptr = ptr.value
+        self.__cuda_array_interface__ = {"shape": (count,), "typestr": typestr,
+                                         "data": (self.ptr, False), "version": 2}
+
+    def __del__(self):
+        if self.ptr:
+            try:
+                lib().bnb8_paged_free(self.ptr)
+            except Exception:  # interpreter teardown: the process frees it
+                pass
+
+
+def paged_empty(count: int, dtype, device=None):
+    """A 1-D tensor of ``count`` elements in paged memory (bnb8_paged_alloc):
+    CUDA managed memory that the driver pages between host and device under
+    device-memory pressure.  It behaves as an ordinary CUDA tensor of
+    ``device``; contents are undefined."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    with torch.cuda.device(device):
+        buf = _PagedBuffer(int(count), dtype)
+        return torch.as_tensor(buf, device=device)
+
+
+def paged_zero_states(specs):
+    """All-zero optimizer states (as ``zero_state``) of several parameters in
+    ONE paged buffer: specs is a list of (p, optim, state_bits, blocksize),
+    all p on one device; returns a list of (s1, s2, absmax1, absmax2), each
+    array a 256-byte aligned slice of the shared buffer, so that one
+    ``paged_prefetch`` call moves the states of all these parameters."""
+    torch = _torch()
+    if not specs:
+        return []
+    device = specs[0][0].device
+    layout, off = [], 0
+    for p, optim, bits, blocksize in specs:
+        if p.device != device:
+            raise ValueError("paged_zero_states: parameters on different devices")
+        entry = []
+        for present, spec in _state_arrays(p.numel(), optim, bits, blocksize):
+            if present is None:
+                entry.append(None)
+                continue
+            count, dtype, value = spec
+            nbytes = count * torch.empty((), dtype=dtype).element_size()
+            entry.append((off, count, dtype, value))
+            off += (nbytes + 255) // 256 * 256
+        layout.append(entry)
+    arena = paged_empty(max(off, 256), torch.uint8, device)
+    out = []
+    for entry in layout:
+        arrays = []
+        for e in entry:
+            if e is None:
+                arrays.append(None)
+                continue
+            o, count, dtype, value = e
+            esize = torch.empty((), dtype=dtype).element_size()
+            arrays.append(arena[o:o + count * esize].view(dtype).fill_(value))
+        out.append(tuple(arrays))
+    return out
+
+
+def paged_prefetch(tensors, device=None, stream=None) -> None:
+    """Migrate paged memory (asynchronously, on ``stream``) to CUDA device
+    ``device`` (default: the tensors' device) or, for ``"cpu"``, to host
+    memory (bnb8_paged_prefetch).  ``tensors`` is one tensor or a list (None
+    entries are skipped); each paged buffer they lie in is moved once, whole:
+    the states that ``paged_zero_states`` packs together take one call."""
+    torch = _torch()
+    if torch.is_tensor(tensors):
+        tensors = [tensors]
+    seen = set()
+    for t in tensors:
+        if t is None:
+            continue
+        st = t.untyped_storage()
+        if st.data_ptr() in seen:
+            continue
+        seen.add(st.data_ptr())
+        if device is not None and torch.device(device).type == "cpu":
+            dev = BNB8_PAGED_HOST
+        else:
+            dev = (t.device if device is None else torch.device(device)).index
+            dev = torch.cuda.current_device() if dev is None else dev
+        _check(lib().bnb8_paged_prefetch(st.data_ptr(), st.nbytes(), dev, _stream(stream)))

@@ -441,7 +441,7 @@ extern "C" {
 
 const char* bnb8_last_error(void) { return g_last_error.c_str(); }
 
-int bnb8_version(void) { return 200; }  // 0.2.0: hparams.flags, blocksize 0
+int bnb8_version(void) { return 300; }  // 0.3.0: paged state
 
 // Dynamic map (see include/bnb8.h).  Levels are emitted directly in ascending
 // order: the negative levels from the largest magnitude down, zero, the
@@ -675,3 +675,71 @@ extern "C" int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const
   const Scalars sc = make_scalars(*hp);
   return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s);
 }
+
+// ---------------------------------------------------------------------------
+// Paged state: state arrays in CUDA managed memory, which the driver pages
+// between host and device memory; the step kernels read them like any other
+// device-accessible memory.  Placement is by explicit prefetch on the step's
+// stream.
+// ---------------------------------------------------------------------------
+namespace {
+
+// BNB8_OK if device `dev` can page managed memory while kernels run
+// (concurrent managed access), which the prefetch and the paged buffers need.
+int check_managed(int dev) {
+  int cma = 0;
+  const cudaError_t e = cudaDeviceGetAttribute(&cma, cudaDevAttrConcurrentManagedAccess, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(concurrent managed access)");
+  if (cma == 0) return fail(BNB8_EUNSUPPORTED, "device %d has no concurrent managed access", dev);
+  return BNB8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bnb8_paged_alloc(size_t bytes, void** out) {
+  if (out == nullptr) return fail(BNB8_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (bytes == 0) return fail(BNB8_EINVAL, "bytes is 0");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const int rc = check_managed(dev);
+  if (rc != BNB8_OK) return rc;
+  void* p = nullptr;
+  e = cudaMallocManaged(&p, bytes, cudaMemAttachGlobal);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocManaged");
+  *out = p;
+  return BNB8_OK;
+}
+
+int bnb8_paged_prefetch(const void* ptr, size_t bytes, int device, struct CUstream_st* stream) {
+  if (bytes == 0) return BNB8_OK;
+  if (ptr == nullptr) return fail(BNB8_EINVAL, "ptr is NULL");
+  if (device < BNB8_PAGED_HOST) return fail(BNB8_EINVAL, "device %d is neither an ordinal nor BNB8_PAGED_HOST", device);
+  int dev = device;
+  if (dev == BNB8_PAGED_HOST) {
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  }
+  const int rc = check_managed(dev);
+  if (rc != BNB8_OK) return rc;
+  cudaMemLocation loc;
+  std::memset(&loc, 0, sizeof(loc));
+  loc.type = device == BNB8_PAGED_HOST ? cudaMemLocationTypeHost : cudaMemLocationTypeDevice;
+  loc.id = device == BNB8_PAGED_HOST ? 0 : device;
+  const cudaError_t e =
+      cudaMemPrefetchAsync(ptr, bytes, loc, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemPrefetchAsync");
+  return BNB8_OK;
+}
+
+int bnb8_paged_free(void* ptr) {
+  if (ptr == nullptr) return BNB8_OK;
+  const cudaError_t e = cudaFree(ptr);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(paged)");
+  return BNB8_OK;
+}
+
+}  // extern "C"

@@ -9,14 +9,25 @@ step computes runs in the library's kernels; this module only keeps the
 per-parameter state and batches parameters into library calls.
 
 Differences from that page, stated: optim_bits defaults to 8 (the classes here
-exist for the 8-bit path); paged state (is_paged) is not provided; blocksize
-(256) and the per-block max_unorm reading (unorm_per_block) are exposed.
+exist for the 8-bit path); blocksize (256) and the per-block max_unorm reading
+(unorm_per_block) are exposed.
+
+Paged optimizers (is_paged=True, and the Paged* classes that the benchmark
+script of "[XPU] Implemented 8bit optimizers in triton #1692" lists): every
+state array lives in paged (CUDA managed) memory, which the driver moves to
+the host when the device runs short.  The states that one step creates share
+one paged buffer, and each step first prefetches the buffers of the
+parameters it updates to their device, on the step's stream: one call per
+buffer, whose pages the step then finds resident instead of faulting them in
+(several times slower).  page_prefetch=False leaves placement to the driver:
+no per-step call, which saves its cost when the states stay resident.
 """
 from __future__ import annotations
 
 import torch
 
-from . import HParams, ParamState, bnb8_create_qmap, step as _step, zero_state
+from . import HParams, ParamState, bnb8_create_qmap, paged_prefetch, paged_zero_states, \
+    step as _step, zero_state
 
 _HPARAM_KEYS = ("lr", "betas", "eps", "weight_decay", "optim_bits", "min_8bit_size", "max_unorm",
                 "skip_zeros", "alpha", "t_alpha", "t_beta3", "blocksize", "unorm_per_block")
@@ -74,7 +85,8 @@ class Optimizer8bit(torch.optim.Optimizer):
     def __init__(self, params, optim="adam", lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
                  weight_decay=0.0, optim_bits=8, min_8bit_size=4096, max_unorm=0.0,
                  skip_zeros=False, alpha=0.0, t_alpha=0, t_beta3=0, blocksize=256,
-                 unorm_per_block=False, manager: OptimManager | None = None):
+                 unorm_per_block=False, is_paged=False, page_prefetch=True,
+                 manager: OptimManager | None = None):
         if optim not in ("adam", "adamw", "momentum", "rmsprop", "adagrad", "lion", "ademamix"):
             raise ValueError(f"unknown optimizer {optim!r}")
         if optim_bits not in (8, 32):
@@ -86,6 +98,8 @@ class Optimizer8bit(torch.optim.Optimizer):
                         unorm_per_block=unorm_per_block)
         super().__init__(params, defaults)
         self.optim = optim
+        self.is_paged = bool(is_paged)
+        self.page_prefetch = bool(page_prefetch)
         self.manager = manager or OptimManager.get_instance()
         self._maps = {}
 
@@ -105,19 +119,36 @@ class Optimizer8bit(torch.optim.Optimizer):
                 (s, u if self.optim in ("adam", "adamw", "ademamix") else None)
         return self._maps[key]
 
-    def _init_state(self, p, cfg) -> dict:
-        """Zero state of parameter p (codes of 0.0, absmax 0, or binary32
-        zeros), allocated on p's device."""
-        bits = 8 if cfg["optim_bits"] == 8 and p.numel() >= cfg["min_8bit_size"] else 32
-        s1, s2, a1, a2 = zero_state(p.data, self.optim, bits, cfg["blocksize"])
-        st = {"step": 0, "state_bits": bits, "state1": s1}
-        if s2 is not None:
-            st["state2"] = s2
-        if a1 is not None:
-            st["absmax1"] = a1
-        if a2 is not None:
-            st["absmax2"] = a2
+    @staticmethod
+    def _bits(p, cfg) -> int:
+        return 8 if cfg["optim_bits"] == 8 and p.numel() >= cfg["min_8bit_size"] else 32
+
+    @staticmethod
+    def _state_dict_of(bits, arrays) -> dict:
+        st = {"step": 0, "state_bits": bits}
+        for key, a in zip(("state1", "state2", "absmax1", "absmax2"), arrays):
+            if a is not None:
+                st[key] = a
         return st
+
+    def _init_states(self, todo, bits_of=None) -> None:
+        """Zero states (codes of 0.0, absmax 0, or binary32 zeros) of the
+        (p, cfg) pairs in todo, on each p's device, with the state bits of
+        bits_of[p] if given, else of cfg; paged: one paged buffer per device
+        for all of them."""
+        bits = {p: (bits_of or {}).get(p) or self._bits(p, cfg) for p, cfg in todo}
+        if not self.is_paged:
+            for p, cfg in todo:
+                self.state[p].update(self._state_dict_of(
+                    bits[p], zero_state(p.data, self.optim, bits[p], cfg["blocksize"])))
+            return
+        by_dev = {}
+        for p, cfg in todo:
+            by_dev.setdefault(p.device, []).append((p, cfg))
+        for items in by_dev.values():
+            specs = [(p.data, self.optim, bits[p], cfg["blocksize"]) for p, cfg in items]
+            for (p, _), arrays in zip(items, paged_zero_states(specs)):
+                self.state[p].update(self._state_dict_of(bits[p], arrays))
 
     # ---- the update ---------------------------------------------------------
     @torch.no_grad()
@@ -127,6 +158,7 @@ class Optimizer8bit(torch.optim.Optimizer):
             with torch.enable_grad():
                 loss = closure()
         batches = {}
+        live, todo = [], []
         for gi, group in enumerate(self.param_groups):
             for p in group["params"]:
                 if p.grad is None:
@@ -138,13 +170,16 @@ class Optimizer8bit(torch.optim.Optimizer):
                 if p.grad.dtype != p.dtype:
                     raise RuntimeError("the gradient must have the parameter's dtype")
                 cfg = self._config(group, p)
-                st = self.state[p]
-                if len(st) == 0:
-                    st.update(self._init_state(p, cfg))
-                st["step"] += 1
-                key = (gi, str(p.device), p.dtype, st["step"],
-                       tuple((k, cfg[k]) for k in _HPARAM_KEYS if k not in ("optim_bits", "min_8bit_size")))
-                batches.setdefault(key, (cfg, []))[1].append(p)
+                live.append((gi, p, cfg))
+                if len(self.state[p]) == 0:
+                    todo.append((p, cfg))
+        self._init_states(todo)
+        for gi, p, cfg in live:
+            st = self.state[p]
+            st["step"] += 1
+            key = (gi, str(p.device), p.dtype, st["step"],
+                   tuple((k, cfg[k]) for k in _HPARAM_KEYS if k not in ("optim_bits", "min_8bit_size")))
+            batches.setdefault(key, (cfg, []))[1].append(p)
         for (gi, dev, dtype, k, _), (cfg, params) in batches.items():
             b1, b2 = cfg["betas"][0], cfg["betas"][1]
             b3 = cfg["betas"][2] if len(cfg["betas"]) > 2 else 0.9999
@@ -154,12 +189,18 @@ class Optimizer8bit(torch.optim.Optimizer):
                          t_beta3=cfg["t_beta3"], skip_zeros=cfg["skip_zeros"],
                          blocksize=cfg["blocksize"], unorm_per_block=cfg["unorm_per_block"])
             states = []
+            stream = torch.cuda.current_stream(params[0].device)
+            if self.is_paged and self.page_prefetch:
+                # each paged buffer once (the batch's states usually share one)
+                paged_prefetch([self.state[p].get(key) for p in params
+                                for key in ("state1", "state2", "absmax1", "absmax2")],
+                               params[0].device, stream)
             for p in params:
                 st = self.state[p]
                 states.append(ParamState(p.data, p.grad, st["state1"], st.get("state2"),
                                          st.get("absmax1"), st.get("absmax2"), st["state_bits"]))
             q1, q2 = self._maps_for(params[0].device)
-            _step(states, hp, q1, q2, stream=torch.cuda.current_stream(params[0].device))
+            _step(states, hp, q1, q2, stream=stream)
         return loss
 
     # ---- checkpoints --------------------------------------------------------
@@ -169,12 +210,26 @@ class Optimizer8bit(torch.optim.Optimizer):
         state tensor keeps the dtype it was saved with, bit for bit."""
         saved = state_dict["state"]
         super().load_state_dict(state_dict)
-        params = [p for g in self.param_groups for p in g["params"]]
+        params = [(g, p) for g in self.param_groups for p in g["params"]]
+        if self.is_paged:
+            # the restored states of each device share one paged buffer again
+            todo = [(params[idx][1], self._config(*params[idx])) for idx in saved
+                    if params[idx][1].is_cuda]
+            self._init_states(todo, {params[idx][1]: st.get("state_bits")
+                                     for idx, st in saved.items()})
         for idx, st in saved.items():
-            p = params[idx]
+            p = params[idx][1]
             for key, val in st.items():
-                if torch.is_tensor(val):
+                if not torch.is_tensor(val):
+                    continue
+                mine = self.state[p].get(key) if self.is_paged and p.is_cuda else None
+                if mine is not None and mine.shape == val.shape and mine.dtype == val.dtype:
+                    mine.copy_(val)
+                else:
                     self.state[p][key] = val.to(device=p.device)
+            for key in ("step", "state_bits"):
+                if key in st:
+                    self.state[p][key] = st[key]
 
 
 def _named(optim, doc_defaults):
@@ -219,3 +274,24 @@ class AdEMAMix8bit(Optimizer8bit):
     """AdEMAMix with 8-bit states (betas = (beta1, beta2, beta3))."""
     __init__ = _named("ademamix", {"betas": (0.9, 0.999, 0.9999), "alpha": 5.0,
                                    "weight_decay": 1e-2})
+
+
+class PagedAdam8bit(Optimizer8bit):
+    """Adam8bit with paged states."""
+    __init__ = _named("adam", {"is_paged": True})
+
+
+class PagedAdamW8bit(Optimizer8bit):
+    """AdamW8bit with paged states."""
+    __init__ = _named("adamw", {"weight_decay": 1e-2, "is_paged": True})
+
+
+class PagedLion8bit(Optimizer8bit):
+    """Lion8bit with paged states."""
+    __init__ = _named("lion", {"lr": 1e-4, "betas": (0.9, 0.99), "is_paged": True})
+
+
+class PagedAdEMAMix8bit(Optimizer8bit):
+    """AdEMAMix8bit with paged states."""
+    __init__ = _named("ademamix", {"betas": (0.9, 0.999, 0.9999), "alpha": 5.0,
+                                   "weight_decay": 1e-2, "is_paged": True})

@@ -26,8 +26,9 @@
  *     launch error; errors raised later by the device surface on the stream.
  *   - The caller owns every buffer.  The library allocates no device or host
  *     memory that outlives a call; scratch comes from a caller-provided
- *     workspace (bnb8_workspace_size).  The one exception is the fixed
- *     scratch array behind bnb8_unorm_static (see there).
+ *     workspace (bnb8_workspace_size).  The exceptions are the fixed
+ *     scratch array behind bnb8_unorm_static and the paged buffers that
+ *     bnb8_paged_alloc hands to the caller (see there).
  *   - Pointers marked "device" must be device-accessible memory of the
  *     current device.  Calls are reentrant; calls on different streams that
  *     touch the same buffers race, as with any CUDA kernel.
@@ -271,6 +272,38 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
 int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
                       const float* qmap1, const float* qmap2, float* out_scale,
                       struct CUstream_st* stream);
+
+/* Paged optimizer state ("optim_overview.md": the paged optimizers and their
+ * is_paged argument; "8-bit Optimizers via Block-wise Quantization" names
+ * paged optimizers among the library's memory savers): state arrays (s1, s2,
+ * absmax1, absmax2) in CUDA managed memory, which the driver pages between
+ * host and device memory under device-memory pressure, so that states larger
+ * than free device memory still step.  The step functions take such arrays
+ * unchanged (any device-accessible pointer); these three calls allocate,
+ * place and free them.  They need a device with concurrent managed access
+ * (cudaDevAttrConcurrentManagedAccess), else BNB8_EUNSUPPORTED. */
+
+/* *out = `bytes` of managed memory (cudaMallocManaged, attached globally),
+ * for the current device; contents undefined.  The caller frees it with
+ * bnb8_paged_free.  Errors: BNB8_EINVAL (out NULL, bytes 0),
+ * BNB8_EUNSUPPORTED, BNB8_ECUDA (out of memory among others). */
+int bnb8_paged_alloc(size_t bytes, void** out);
+
+/* Migrates [ptr, ptr + bytes) of a bnb8_paged_alloc buffer, asynchronously
+ * on `stream`, to device `device` (an ordinal >= 0), or to host memory for
+ * device == BNB8_PAGED_HOST.  The paged optimizers call it for every state
+ * array, to the device, before each step on the step's stream, so the step
+ * kernel finds its pages resident instead of faulting them in one by one.
+ * Migration is a placement hint: the data stay valid wherever they live.
+ * bytes == 0 does nothing.  Errors: BNB8_EINVAL (ptr NULL with bytes > 0,
+ * device < -1), BNB8_EUNSUPPORTED, BNB8_ECUDA. */
+int bnb8_paged_prefetch(const void* ptr, size_t bytes, int device, struct CUstream_st* stream);
+
+enum { BNB8_PAGED_HOST = -1 };
+
+/* Frees a bnb8_paged_alloc buffer (NULL: nothing).  Like cudaFree, it waits
+ * for the device to finish work that may use the buffer. */
+int bnb8_paged_free(void* ptr);
 
 #ifdef __cplusplus
 }

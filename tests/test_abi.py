@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 11
+    assert len(names) == 14
     assert sorted(bnb8.EXPORTS) == names
     for name in names:
         assert hasattr(L, name), name
@@ -180,3 +180,15 @@ def test_launch_block_limit(L):
     t = _tensor(n=(1 << 31) * 256 + 1)
     assert _call2(L, [t], _hp()) == bnb8.BNB8_EUNSUPPORTED
     assert b"blocks in one launch" in L.bnb8_last_error()
+
+
+def test_paged_args_rejected_before_the_device(L):
+    out = ctypes.c_void_p(1234)
+    assert L.bnb8_paged_alloc(0, ctypes.byref(out)) == bnb8.BNB8_EINVAL
+    assert out.value is None  # cleared on failure
+    assert L.bnb8_paged_alloc(16, None) == bnb8.BNB8_EINVAL
+    assert L.bnb8_paged_prefetch(None, 16, 0, None) == bnb8.BNB8_EINVAL
+    assert L.bnb8_paged_prefetch(ctypes.c_void_p(4096), 16, -2, None) == bnb8.BNB8_EINVAL
+    assert b"BNB8_PAGED_HOST" in L.bnb8_last_error()
+    assert L.bnb8_paged_prefetch(None, 0, 0, None) == bnb8.BNB8_OK  # nothing to move
+    assert L.bnb8_paged_free(None) == bnb8.BNB8_OK

@@ -17,7 +17,8 @@ def test_min_8bit_size_and_overrides():
     mgr.override_config(ps[2], "optim_bits", 32)
     opt = O.Adam8bit(ps, manager=mgr)
     g = opt.param_groups[0]
-    st = [opt._init_state(p, opt._config(g, p)) for p in ps]
+    opt._init_states([(p, opt._config(g, p)) for p in ps])
+    st = [opt.state[p] for p in ps]
     assert [s["state_bits"] for s in st] == [8, 32, 32]
     assert st[0]["state1"].dtype == torch.uint8 and st[0]["absmax1"].numel() == 8192 // 256
     assert torch.all(st[0]["state1"] == 127)          # the signed map's 0.0
@@ -28,7 +29,8 @@ def test_min_8bit_size_and_overrides():
 def test_tensorwise_state_has_one_absmax_per_state():
     opt = O.AdEMAMix8bit(_params()[:1], blocksize=0, manager=O.OptimManager())
     p = opt.param_groups[0]["params"][0]
-    st = opt._init_state(p, opt._config(opt.param_groups[0], p))
+    opt._init_states([(p, opt._config(opt.param_groups[0], p))])
+    st = opt.state[p]
     assert st["absmax1"].numel() == 2 and st["absmax2"].numel() == 1
     assert st["state1"].numel() == 2 * p.numel()
 
@@ -40,3 +42,12 @@ def test_config_errors():
         O.Optimizer8bit(_params(), optim="sgd")
     with pytest.raises(ValueError):
         O.Adam8bit(_params(), optim_bits=16)
+
+
+def test_paged_classes():
+    for name in ("Adam8bit", "AdamW8bit", "Lion8bit", "AdEMAMix8bit"):
+        paged = getattr(O, "Paged" + name)(_params(), manager=O.OptimManager())
+        plain = getattr(O, name)(_params(), manager=O.OptimManager())
+        assert paged.is_paged and paged.page_prefetch and not plain.is_paged
+        assert paged.optim == plain.optim and paged.defaults == plain.defaults
+    assert not O.PagedAdam8bit(_params(), page_prefetch=False).page_prefetch
