@@ -273,12 +273,12 @@ int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const bnb8_hpara
                       const float* qmap1, const float* qmap2, float* out_scale,
                       struct CUstream_st* stream);
 
-/* Paged optimizer state ("optim_overview.md": the paged optimizers and their
- * is_paged argument; "8-bit Optimizers via Block-wise Quantization" names
- * paged optimizers among the library's memory savers): state arrays (s1, s2,
- * absmax1, absmax2) in CUDA managed memory, which the driver pages between
- * host and device memory under device-memory pressure, so that states larger
- * than free device memory still step.  The step functions take such arrays
+/* Paged optimizer state ("optim_overview.md": the is_paged argument of the
+ * optimizers; "[XPU] Implemented 8bit optimizers in triton #1692", benchmark
+ * script: PagedAdam8bit, PagedAdamW8bit, PagedLion8bit, PagedAdEMAMix8bit):
+ * state arrays (s1, s2, absmax1, absmax2) in CUDA managed memory, which the
+ * driver pages between host and device memory under device-memory pressure,
+ * so that states larger than free device memory still step.  The step functions take such arrays
  * unchanged (any device-accessible pointer); these three calls allocate,
  * place and free them.  They need a device with concurrent managed access
  * (cudaDevAttrConcurrentManagedAccess), else BNB8_EUNSUPPORTED. */
