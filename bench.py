@@ -561,7 +561,9 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     memory, every step.  The work is cut into four launches of about equal
     size (e2e_groups), so that the upload of group i+1, the step on group i
     and the read-back of group i-1 run concurrently on three streams; each
-    launch is a Stepper (arguments marshalled once)."""
+    launch is a Stepper (arguments marshalled once).  The device gradient is
+    double-buffered, so the next step's uploads start while this step's
+    launches still read the other buffer and the link never drains."""
     import torch
     if wl.elements > (1 << 28):
         steps = max(2, min(args.steps, 5))
@@ -571,40 +573,46 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     host_p = [torch.empty(n, dtype=tdt, pin_memory=True) for n in wl.sizes]
     for hg, ps in zip(host_g, params):
         hg.copy_(ps.g if ps.g is not None else torch.zeros_like(ps.p))
-    dev_g = [torch.empty_like(ps.p) for ps in params]
-    for ps, dg in zip(params, dev_g):
-        ps.g = dg
-    groups = e2e_groups(bnb8, params, wl, 4)
     hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **wl.hp)
-    steppers = [bnb8.Stepper([pc for _, _, pc in grp], hp0, q1, q2,
-                             workspace=workspace if ws_bytes else None) for grp in groups]
+    dev_g, groups, steppers = [], [], []
+    for buf in range(2):
+        dev_g.append([torch.empty_like(ps.p) for ps in params])
+        for ps, dg in zip(params, dev_g[buf]):
+            ps.g = dg
+        groups.append(e2e_groups(bnb8, params, wl, 4))
+        steppers.append([bnb8.Stepper([pc for _, _, pc in grp], hp0, q1, q2,
+                                      workspace=workspace if ws_bytes else None)
+                         for grp in groups[buf]])
+    ngroups = len(groups[0])
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_up = [torch.cuda.Event() for _ in groups]
-    ev_done = [torch.cuda.Event() for _ in groups]
-    ev_back = [torch.cuda.Event() for _ in groups]
+    ev_up = [torch.cuda.Event() for _ in range(ngroups)]
+    ev_done = [[torch.cuda.Event() for _ in range(ngroups)] for _ in range(2)]
+    ev_back = [torch.cuda.Event() for _ in range(ngroups)]
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
     for k in range(steps):
         step_no[0] += 1
-        for c, grp in enumerate(groups):
+        buf = k % 2
+        for c, grp in enumerate(groups[buf]):
             with torch.cuda.stream(s_in):
+                # this buffer's previous readers (two steps back) are done
+                s_in.wait_event(ev_done[buf][c])
                 for i, (lo, hi), _ in grp:
-                    dev_g[i][lo:hi].copy_(host_g[i][lo:hi], non_blocking=True)
+                    dev_g[buf][i][lo:hi].copy_(host_g[i][lo:hi], non_blocking=True)
                 ev_up[c].record(s_in)
             stream.wait_event(ev_up[c])
             if k > 0:                           # p of this group is still being read back
                 stream.wait_event(ev_back[c])
-            steppers[c](step_no[0], stream)
-            ev_done[c].record(stream)
-            s_out.wait_event(ev_done[c])
+            steppers[buf][c](step_no[0], stream)
+            ev_done[buf][c].record(stream)
+            s_out.wait_event(ev_done[buf][c])
             with torch.cuda.stream(s_out):
                 for i, (lo, hi), pc in grp:
                     host_p[i][lo:hi].copy_(pc.p, non_blocking=True)
                 ev_back[c].record(s_out)
-        # the next step's uploads overwrite g: wait until this step consumed it
-        s_in.wait_stream(stream)
     s_out.wait_stream(s_in)
+    s_out.wait_stream(stream)
     end.record(s_out)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
@@ -612,8 +620,8 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     return {"value": round(wl.elements / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": wl.elements * esz, "d2h_bytes_per_step": wl.elements * esz,
             "ms_per_step": round(ms, 4), "steps": steps,
-            "pipeline": f"{len(groups)} launches of about equal size, upload / step / read-back "
-                        "on three streams"}
+            "pipeline": f"{ngroups} launches of about equal size, upload / step / read-back "
+                        "on three streams, device gradient double-buffered"}
 
 
 def run_codec(args, wl):
