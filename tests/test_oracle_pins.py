@@ -575,6 +575,45 @@ def test_skip_zeros_identities(optim, state_bits, dtype):
 
 
 @pytest.mark.parametrize("optim", sorted(MAPS))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_rows_over_zero_states_are_fixed_points(optim, dtype):
+    """Without decay, a block whose gradient is all zero (+0 and -0) over zero
+    states comes out of a plain step (skip_zeros off) exactly as skip_zeros
+    would leave it: p, codes and absmax unchanged.  Every ratio there is a
+    signed zero over eps, so the update direction is zero."""
+    q1, q2 = MAPS[optim]
+    n, B = 8 * 256, 256
+    g = workloads.normal(n, 1e-2, 90)
+    rng = np.random.default_rng(91)
+    zero_blocks = [1, 2, 5]
+    for b in zero_blocks:
+        g[b * B:(b + 1) * B] = np.where(rng.random(B) < 0.5, 0.0, -0.0)
+    g = oracle.to_storage(g, dtype)
+    base = oracle.TensorState(oracle.to_storage(workloads.normal(n, 0.1, 92), dtype),
+                              *oracle.zero_state(optim, n, 8, B, q1, q2), 8)
+    hpkw = dict(optim=optim, step=1, weight_decay=0.0, alpha=5.0)
+    on, off = base.copy(), base.copy()
+    oracle.step(oracle.HParams(skip_zeros=True, **hpkw), on, g, dtype, B, q1, q2)
+    oracle.step(oracle.HParams(skip_zeros=False, **hpkw), off, g, dtype, B, q1, q2)
+    for b in zero_blocks:
+        sl = slice(b * B, (b + 1) * B)
+        np.testing.assert_array_equal(off.p[sl], base.p[sl])
+        np.testing.assert_array_equal(off.p[sl], on.p[sl])
+    reps = 2 if optim == "ademamix" else 1
+    for c_off, c_b, a_off, a_b, r in [(off.s1, base.s1, off.absmax1, base.absmax1, reps),
+                                      (off.s2, base.s2, off.absmax2, base.absmax2, 1)]:
+        if c_off is None:
+            continue
+        for k in range(r):
+            for b in zero_blocks:
+                sl = slice(k * n + b * B, k * n + (b + 1) * B)
+                np.testing.assert_array_equal(c_off[sl], c_b[sl])
+                assert a_off[k * (n // B) + b] == 0.0
+    # the live blocks did move
+    assert not np.array_equal(off.p[:B], base.p[:B])
+
+
+@pytest.mark.parametrize("optim", sorted(MAPS))
 def test_skip_zeros_without_zeros_equals_plain(optim):
     q1, q2 = MAPS[optim]
     n, B = 1000, 256
