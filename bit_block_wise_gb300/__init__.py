@@ -24,6 +24,8 @@ BNB8_OK, BNB8_EINVAL, BNB8_EUNSUPPORTED, BNB8_ECUDA, BNB8_EWORKSPACE = 0, 1, 2, 
 BNB8_F32, BNB8_BF16, BNB8_F16 = 0, 1, 2
 BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX = range(7)
 BNB8_UNORM_PER_BLOCK = 1
+BNB8_TEST_STALL_WAIT = 0x100
+BNB8_STATUS_WAIT_TIMEOUT = 1
 BNB8_PAGED_HOST = -1
 
 OPTIMS = {"adam": BNB8_ADAM, "adamw": BNB8_ADAMW, "momentum": BNB8_MOMENTUM,
@@ -36,10 +38,11 @@ NSTATES = {"adam": 2, "adamw": 2, "momentum": 1, "rmsprop": 1, "adagrad": 1, "li
 MIN_8BIT_SIZE = 4096
 
 # every symbol include/bnb8.h declares
-EXPORTS = ("bnb8_last_error", "bnb8_version", "bnb8_create_qmap", "bnb8_quantize_blockwise",
+EXPORTS = ("bnb8_last_error", "bnb8_version", "bnb8_create_qmap", "bnb8_qmap_code",
+           "bnb8_quantize_blockwise",
            "bnb8_dequantize_blockwise", "bnb8_workspace_size", "bnb8_step_2state",
            "bnb8_step_1state", "bnb8_step_ademamix", "bnb8_unorm", "bnb8_unorm_static",
-           "bnb8_paged_alloc", "bnb8_paged_prefetch", "bnb8_paged_free")
+           "bnb8_paged_alloc", "bnb8_paged_prefetch", "bnb8_paged_free", "bnb8_device_status")
 
 
 class Bnb8Tensor(ctypes.Structure):
@@ -76,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.bnb8_last_error.argtypes = []
         L.bnb8_version.restype = i32
         L.bnb8_create_qmap.argtypes = [i32, vp]
+        L.bnb8_qmap_code.argtypes = [vp, ctypes.c_float, ctypes.POINTER(ctypes.c_uint8)]
         L.bnb8_quantize_blockwise.argtypes = [vp, i32, i64, vp, i32, vp, vp, vp]
         L.bnb8_dequantize_blockwise.argtypes = [vp, vp, vp, i32, i64, vp, i32, vp]
         L.bnb8_workspace_size.argtypes = [ctypes.POINTER(Bnb8Tensor), i32,
@@ -94,6 +98,7 @@ def lib() -> ctypes.CDLL:
         L.bnb8_paged_alloc.argtypes = [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]
         L.bnb8_paged_prefetch.argtypes = [vp, ctypes.c_size_t, i32, vp]
         L.bnb8_paged_free.argtypes = [vp]
+        L.bnb8_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         for name in EXPORTS:
             if name not in ("bnb8_last_error", "bnb8_version", "bnb8_workspace_size"):
                 getattr(L, name).restype = i32
@@ -155,9 +160,10 @@ class HParams:
     skip_zeros: bool = False
     blocksize: int = 256
     unorm_per_block: bool = False  # max_unorm per block (BNB8_UNORM_PER_BLOCK)
+    extra_flags: int = 0           # other hparams.flags bits (BNB8_TEST_STALL_WAIT)
 
     def c(self, dtype_code: int) -> Bnb8Hparams:
-        flags = BNB8_UNORM_PER_BLOCK if self.unorm_per_block else 0
+        flags = (BNB8_UNORM_PER_BLOCK if self.unorm_per_block else 0) | int(self.extra_flags)
         return Bnb8Hparams(OPTIMS[self.optim], dtype_code, self.blocksize, int(bool(self.skip_zeros)),
                            self.lr, self.beta1, self.beta2, self.beta3, self.alpha, self.eps,
                            self.weight_decay, self.gnorm_scale, self.max_unorm, flags,
@@ -197,12 +203,32 @@ def bnb8_version() -> int:
     return int(lib().bnb8_version())
 
 
+def bnb8_device_status(clear: bool = False) -> int:
+    """The library's device status word of the current device (bits
+    BNB8_STATUS_*), read after the device finishes its work; clear zeroes it."""
+    out = ctypes.c_uint32()
+    _check(lib().bnb8_device_status(ctypes.byref(out), int(bool(clear))))
+    return int(out.value)
+
+
 def bnb8_create_qmap(is_signed: bool):
     """The 256-level dynamic map as a float32 CPU tensor."""
     torch = _torch()
     out = torch.empty(256, dtype=torch.float32)
     _check(lib().bnb8_create_qmap(int(bool(is_signed)), out.data_ptr()))
     return out
+
+
+def bnb8_qmap_code(qmap, x: float) -> int:
+    """The code of the normalised value x under a map (any 256-element
+    float32 tensor or array; copied to the host)."""
+    torch = _torch()
+    q = torch.as_tensor(qmap).detach().to("cpu", torch.float32).contiguous()
+    if q.numel() != 256:
+        raise ValueError(f"a map has 256 levels, not {q.numel()}")
+    out = ctypes.c_uint8()
+    _check(lib().bnb8_qmap_code(q.data_ptr(), float(x), ctypes.byref(out)))
+    return int(out.value)
 
 
 def bnb8_quantize_blockwise(x, qmap, blocksize: int = 256, codes=None, absmax=None, stream=None):
@@ -377,16 +403,35 @@ def split_blocks(ps: ParamState, blocksize: int, nchunks: int):
     return ranges, pieces
 
 
-def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256, paged: bool = False):
-    """Allocate the all-zero optimizer state of parameter p (codes of 0.0 in
-    the signed / unsigned maps of bnb8_create_qmap, absmax 0).  blocksize 0:
+_ZERO_CODES = {}
+
+
+def _zero_codes(optim: str, qmap1=None, qmap2=None):
+    """(code of 0.0 under qmap1, under qmap2): maps default to the library's
+    (bnb8_create_qmap: signed for s1 except RMSprop and Adagrad, unsigned for
+    s2); the codes come from the library's nearest-level rule."""
+    def code(q, signed):
+        if q is not None:
+            return bnb8_qmap_code(q, 0.0)
+        if signed not in _ZERO_CODES:
+            _ZERO_CODES[signed] = bnb8_qmap_code(bnb8_create_qmap(signed), 0.0)
+        return _ZERO_CODES[signed]
+    return code(qmap1, optim not in ("rmsprop", "adagrad")), code(qmap2, False)
+
+
+def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256, paged: bool = False,
+               qmap1=None, qmap2=None):
+    """Allocate the all-zero optimizer state of parameter p: every code is the
+    code of 0.0 in its map (qmap1 / qmap2; by default the maps of
+    bnb8_create_qmap the optimizer uses), every absmax 0.  blocksize 0:
     tensor-wise quantization, one absmax per state.  paged: the state arrays
     share one paged (managed) buffer (``paged_zero_states``)."""
     if paged:
-        return paged_zero_states([(p, optim, state_bits, blocksize)])[0]
+        return paged_zero_states([(p, optim, state_bits, blocksize, qmap1, qmap2)])[0]
     torch = _torch()
     out = []
-    for present, spec in _state_arrays(p.numel(), optim, state_bits, blocksize):
+    zeros = _zero_codes(optim, qmap1, qmap2) if state_bits == 8 else (0, 0)
+    for present, spec in _state_arrays(p.numel(), optim, state_bits, blocksize, zeros):
         if present is None:
             out.append(None)
             continue
@@ -395,9 +440,10 @@ def zero_state(p, optim: str, state_bits: int = 8, blocksize: int = 256, paged: 
     return tuple(out)
 
 
-def _state_arrays(n: int, optim: str, state_bits: int, blocksize: int):
+def _state_arrays(n: int, optim: str, state_bits: int, blocksize: int, zeros=(0, 0)):
     """(s1, s2, absmax1, absmax2) of an n-element parameter as
-    (present, (count, dtype, zero value)) pairs."""
+    (present, (count, dtype, zero value)) pairs; zeros = the codes of 0.0 of
+    s1 and s2 (8-bit state)."""
     torch = _torch()
     k = NSTATES[optim]
     m = 2 if optim == "ademamix" else 1
@@ -405,9 +451,8 @@ def _state_arrays(n: int, optim: str, state_bits: int, blocksize: int):
         return [(1, (n * m, torch.float32, 0.0)), (1 if k >= 2 else None, (n, torch.float32, 0.0)),
                 (None, None), (None, None)]
     nb = 1 if blocksize == 0 else (n + blocksize - 1) // blocksize  # 0: tensor-wise
-    zero1 = 127 if optim not in ("rmsprop", "adagrad") else 0  # code of 0.0 in the map of s1
     two = 1 if k >= 2 else None
-    return [(1, (n * m, torch.uint8, zero1)), (two, (n, torch.uint8, 0)),
+    return [(1, (n * m, torch.uint8, zeros[0])), (two, (n, torch.uint8, zeros[1])),
             (1, (nb * m, torch.float32, 0.0)), (two, (nb, torch.float32, 0.0))]
 
 
@@ -458,17 +503,21 @@ def paged_zero_states(specs):
     ONE paged buffer: specs is a list of (p, optim, state_bits, blocksize),
     all p on one device; returns a list of (s1, s2, absmax1, absmax2), each
     array a 256-byte aligned slice of the shared buffer, so that one
-    ``paged_prefetch`` call moves the states of all these parameters."""
+    ``paged_prefetch`` call moves the states of all these parameters.  A spec
+    may add (qmap1, qmap2) as in ``zero_state``."""
     torch = _torch()
     if not specs:
         return []
     device = specs[0][0].device
     layout, off = [], 0
-    for p, optim, bits, blocksize in specs:
+    for spec_in in specs:
+        p, optim, bits, blocksize = spec_in[:4]
+        qm1, qm2 = (tuple(spec_in[4:6]) + (None, None))[:2]
         if p.device != device:
             raise ValueError("paged_zero_states: parameters on different devices")
         entry = []
-        for present, spec in _state_arrays(p.numel(), optim, bits, blocksize):
+        zeros = _zero_codes(optim, qm1, qm2) if bits == 8 else (0, 0)
+        for present, spec in _state_arrays(p.numel(), optim, bits, blocksize, zeros):
             if present is None:
                 entry.append(None)
                 continue

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbnb8.so")
 SOURCES = ["bnb8_api.cu", "k_quant.cu", "k_step_adam.cu", "k_step_1state.cu", "k_step_ademamix.cu"]
-HEADERS = ["bnb8_internal.h", "bnb8_device.cuh", "k_step8.cuh", "k_step32.cuh"]
+HEADERS = ["bnb8_internal.h", "bnb8_device.cuh", "k_step8.cuh", "k_step8_ring.cuh", "k_step32.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

@@ -4,6 +4,7 @@
 // with -ffp-contract=off so every scalar below is one fixed expression.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -57,17 +58,21 @@ int nmaps(int optim) {
   return (optim == BNB8_ADAM || optim == BNB8_ADAMW || optim == BNB8_ADEMAMIX) ? 2 : 1;
 }
 
-// SM count of the current device (cached per device).
+// SM count of the current device (cached per device; a larger ordinal than
+// the cache holds is queried on every call).
 int sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cache[dev] == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  const bool cached = dev < kMaxDevices;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
-  return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (cached) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // ---- per-step scalars -------------------------------------------------------
@@ -140,8 +145,9 @@ int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int*
                 hp->blocksize);
   if (hp->blocksize == 0 && (hp->flags & BNB8_UNORM_PER_BLOCK) != 0)
     return fail(BNB8_EINVAL, "BNB8_UNORM_PER_BLOCK needs blocks (blocksize 0 is tensor-wise)");
-  if ((hp->flags & ~BNB8_UNORM_PER_BLOCK) != 0)
-    return fail(BNB8_EINVAL, "hparams.flags: unknown bits 0x%x", hp->flags & ~BNB8_UNORM_PER_BLOCK);
+  const int known = BNB8_UNORM_PER_BLOCK | BNB8_TEST_STALL_WAIT;
+  if ((hp->flags & ~known) != 0)
+    return fail(BNB8_EINVAL, "hparams.flags: unknown bits 0x%x", hp->flags & ~known);
   if (hp->step < 1) return fail(BNB8_EINVAL, "step must be >= 1 (got %lld)", (long long)hp->step);
   if (hp->t_alpha < 0 || hp->t_beta3 < 0) return fail(BNB8_EINVAL, "t_alpha / t_beta3 must be >= 0");
   if (!(hp->max_unorm >= 0.0f) || std::isinf(hp->max_unorm))
@@ -149,15 +155,15 @@ int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int*
   return BNB8_OK;
 }
 
-// Validate one descriptor; sets *vec to whether every stream is aligned for
-// the vector path.
-int check_tensor(const bnb8_tensor& t, int i, const bnb8_hparams& hp, bool* vec) {
+// Validate one descriptor; sets *vec to DevTensor::vec_ok's bits: 1 if every
+// stream is aligned for the vector path, 3 if also for whole-chunk bulk copies.
+int check_tensor(const bnb8_tensor& t, int i, const bnb8_hparams& hp, int* vec) {
   if (t.n < 0) return fail(BNB8_EINVAL, "tensor %d: n < 0", i);
   if (t.reserved != 0) return fail(BNB8_EINVAL, "tensor %d: reserved must be 0", i);
   if (t.state_bits != 8 && t.state_bits != 32)
     return fail(BNB8_EINVAL, "tensor %d: state_bits must be 8 or 32 (got %d)", i, t.state_bits);
   if (t.n > (int64_t(1) << 50)) return fail(BNB8_EINVAL, "tensor %d: n too large", i);
-  *vec = false;
+  *vec = 0;
   if (t.n == 0) return BNB8_OK;
   const int ns = nstates(hp.optim);
   const int es = elem_size(hp.dtype);
@@ -176,14 +182,19 @@ int check_tensor(const bnb8_tensor& t, int i, const bnb8_hparams& hp, bool* vec)
       return fail(BNB8_EINVAL, "tensor %d: 32-bit states must be 4-byte aligned", i);
   }
   bool v = aligned(t.p, 16) && aligned(t.g, 16);
+  bool bulk = false;
   if (t.state_bits == 8) {
+    // bulk copies of whole chunks want 16-byte aligned code streams too
+    // (AdEMAMix's m2 half starts n bytes into s1)
+    bulk = v && aligned(t.s1, 16) && (ns < 2 || aligned(t.s2, 16)) &&
+           (hp.optim != BNB8_ADEMAMIX || t.n % 16 == 0);
     v = v && aligned(t.s1, 8) && (ns < 2 || aligned(t.s2, 8));
     if (hp.optim == BNB8_ADEMAMIX) v = v && (t.n % 8 == 0);
   } else {
     v = v && aligned(t.s1, 16) && (ns < 2 || aligned(t.s2, 16));
     if (hp.optim == BNB8_ADEMAMIX) v = v && (t.n % 4 == 0);
   }
-  *vec = v;
+  *vec = v ? (bulk ? 3 : 1) : 0;
   return BNB8_OK;
 }
 
@@ -206,10 +217,10 @@ int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
   plan->vec.assign(nt, 0);
   bool any8 = false;
   for (int i = 0; i < nt; ++i) {
-    bool v = false;
+    int v = 0;
     const int rc = check_tensor(ts[i], i, hp, &v);
     if (rc != BNB8_OK) return rc;
-    plan->vec[i] = v ? 1 : 0;
+    plan->vec[i] = static_cast<char>(v);
     if (ts[i].n > 0 && ts[i].state_bits == 8) any8 = true;
   }
   if (any8) {
@@ -252,6 +263,33 @@ int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The library's device status word (one per device that loads the library):
+// kernels or-in kStatus* bits, bnb8_device_status reads and clears it.
+__device__ uint32_t g_device_status;
+
+// Device address of g_device_status on the current device, looked up once per
+// device (atomics: host threads may race on the first call) and cached.
+int device_status_addr(uint32_t** out) {
+  static std::atomic<uint32_t*> addr[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  uint32_t* a = cached ? addr[dev].load(std::memory_order_acquire) : nullptr;
+  if (a == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device status)");
+    a = static_cast<uint32_t*>(ptr);
+    if (cached) addr[dev].store(a, std::memory_order_release);
+  }
+  *out = a;
+  return BNB8_OK;
+}
+
+// Bound of every wait for an async copy inside the step kernels.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
 // Workspace layout: [per-tensor max_unorm multipliers][per-block partials]
 // when the per-tensor pre-pass runs, then [4 words per tensor] of tensor-wise
 // absmax accumulators when blocksize is 0.
@@ -286,6 +324,9 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
                  std::isfinite(sc.b2) && std::isfinite(sc.omb1) && std::isfinite(sc.omb2) &&
                  std::isfinite(hp.gnorm_scale);
   a.tensorwise = hp.blocksize == 0 ? 1 : 0;
+  a.nsm = sm_count();
+  a.stall_test = (hp.flags & BNB8_TEST_STALL_WAIT) != 0 ? 1 : 0;
+  a.wait_ns = kWaitLimitNs;
   a.log2B = log2B;
   a.ntensors = static_cast<int32_t>(c.idx.size());
   a.total_blocks = c.total_blocks;
@@ -305,7 +346,8 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
     d.first_block = fb;
     d.index = c.idx[k];
     d.vec_ok = plan.vec[c.idx[k]];
-    fb += (t.n + (int64_t(1) << log2B) - 1) >> log2B;
+    d.nblocks = static_cast<int32_t>((t.n + (int64_t(1) << log2B) - 1) >> log2B);
+    fb += d.nblocks;
   }
   return a;
 }
@@ -318,12 +360,15 @@ cudaError_t launch_family(int bits, int optim, int dtype, int mode, const StepAr
 }
 
 int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int log2B) {
-  static int cache[2][7][3][5] = {};
-  int& c = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
+  // resident CTAs per SM of each kernel (the same on every device of a process)
+  static std::atomic<int> cache[2][7][3][5];
+  std::atomic<int>& slot = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
+  int c = slot.load(std::memory_order_relaxed);
   if (c == 0) {
     if (optim == BNB8_ADAM || optim == BNB8_ADAMW) c = ctas_step_adam(bits, optim, dtype, mode);
     else if (optim == BNB8_ADEMAMIX) c = ctas_step_ademamix(bits, optim, dtype, mode);
     else c = ctas_step_1state(bits, optim, dtype, mode);
+    slot.store(c, std::memory_order_relaxed);
   }
   const int groups_per_cta = kThreads / ((1 << log2B) >> 3);
   const int64_t need = (total_blocks + groups_per_cta - 1) / groups_per_cta;
@@ -389,6 +434,9 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
   if (need > 0 && (ws == nullptr || !aligned(ws, 256) || ws_bytes < need))
     return fail(BNB8_EWORKSPACE, "%s needs a 256-byte aligned workspace of %zu bytes (got %zu)",
                 prepass ? "max_unorm" : "tensor-wise quantization", need, ws_bytes);
+  uint32_t* status = nullptr;
+  rc = device_status_addr(&status);
+  if (rc != BNB8_OK) return rc;
   uint32_t* tw_acc = tw ? reinterpret_cast<uint32_t*>(
                               static_cast<char*>(ws) + (prepass ? workspace_bytes_for(nt, plan.all_blocks) : 0))
                         : nullptr;
@@ -417,6 +465,7 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
     StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
     a.clip = clip;
     a.tw_acc = tw_acc;
+    a.status = status;
     const int m = (tw && c.bits == 8) ? MODE_TWSTEP : mode;
     const int grid = grid_for(c.bits, hp->optim, hp->dtype, m, c.total_blocks, log2B);
     const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, m, a, grid, stream);
@@ -472,6 +521,24 @@ int bnb8_create_qmap(int is_signed, float* out) {
   }
   out[i++] = 1.0f;
   return i == 256 ? BNB8_OK : fail(BNB8_EUNSUPPORTED, "internal: map has %d levels", i);
+}
+
+// Nearest-level code on the host: the count of binary32 midpoints below x,
+// each midpoint formed as (q[j] + q[j+1]) * 0.5 with one rounding per
+// operation, as the kernels form them.
+int bnb8_qmap_code(const float* qmap, float x, uint8_t* code) {
+  if (qmap == nullptr || code == nullptr) return fail(BNB8_EINVAL, "qmap and code must not be NULL");
+  if (std::isnan(x)) return fail(BNB8_EINVAL, "x is NaN");
+  for (int j = 0; j < 255; ++j)
+    if (!(qmap[j] < qmap[j + 1]))
+      return fail(BNB8_EINVAL, "qmap is not strictly ascending at index %d", j);
+  int c = 0;
+  for (int j = 0; j < 255; ++j) {
+    const float mid = (qmap[j] + qmap[j + 1]) * 0.5f;
+    if (mid < x) ++c;
+  }
+  *code = static_cast<uint8_t>(c);
+  return BNB8_OK;
 }
 
 int bnb8_quantize_blockwise(const void* x, int dtype, int64_t n, const float* qmap, int blocksize,
@@ -551,6 +618,23 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
   return (prepass ? workspace_bytes_for(ntensors, blocks) : 0) + (tw ? tw_bytes_for(ntensors) : 0);
 }
 
+int bnb8_device_status(uint32_t* status, int clear) {
+  if (status == nullptr) return fail(BNB8_EINVAL, "status is NULL");
+  *status = 0u;
+  uint32_t* addr = nullptr;
+  int rc = device_status_addr(&addr);
+  if (rc != BNB8_OK) return rc;
+  cudaError_t e = cudaMemcpy(status, addr, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  if (clear) {
+    e = cudaMemset(addr, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status");
+  }
+  return BNB8_OK;
+}
+
 int bnb8_step_2state(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
                      const float* qmap1, const float* qmap2, void* workspace,
                      size_t workspace_bytes, struct CUstream_st* stream) {
@@ -623,19 +707,24 @@ __device__ __align__(256) float2 g_static_scratch[kStaticScratchBlocks];
 // Device address of g_static_scratch on the current device, looked up once per
 // device (with that device current) and cached.  Host code must not use the
 // array's name as a pointer: on the host it only stands in for the symbol.
+// The cache entries are atomics: host threads making their first call on a
+// device at the same time both look the address up and store the same value.
 int static_scratch(float2** out) {
-  static float2* addr[64] = {nullptr};
+  static std::atomic<float2*> addr[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(BNB8_EUNSUPPORTED, "device ordinal %d out of range", dev);
-  if (addr[dev] == nullptr) {
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(BNB8_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  float2* a = addr[dev].load(std::memory_order_acquire);
+  if (a == nullptr) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    addr[dev] = static_cast<float2*>(ptr);
+    a = static_cast<float2*>(ptr);
+    addr[dev].store(a, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = a;
   return BNB8_OK;
 }
 

@@ -5,7 +5,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace bnb8 {
+
+// Per-device one-time set-up (a kernel's shared-memory limit, the device
+// address of a symbol) is cached in arrays of kMaxDevices atomics, so that
+// host threads calling the library at the same time never race on the cache.
+// Devices with a larger ordinal skip the cache and redo the set-up per call.
+constexpr int kMaxDevices = 64;
+
+// cudaFuncSetAttribute(fn, MaxDynamicSharedMemorySize, bytes) once per device.
+inline cudaError_t set_smem_limit_once(const void* fn, int bytes,
+                                       std::atomic<unsigned char>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
+  return e;
+}
+
+// Bits of the library's device status word (StepArgs::status).
+constexpr uint32_t kStatusWaitTimeout = 1u;  // a bounded wait for an async copy ran out
 
 constexpr int kThreads = 512;       // threads per CTA of every step / quantize kernel
 constexpr int kMaxTensors = 96;     // descriptors per launch (kernel parameter space)
@@ -32,7 +56,11 @@ struct DevTensor {
   int64_t n;
   int64_t first_block;  // index of the tensor's first block in the launch
   int32_t index;        // position in the caller's tensor list (clip / out_scale slot)
-  int32_t vec_ok;       // every stream of this tensor is aligned for vector access
+  // bit 0: every stream of this tensor is aligned for vector access; bit 1:
+  // also for 16-byte bulk copies of whole 256-element chunks
+  int32_t vec_ok;
+  int32_t nblocks;      // ceil(n / B)
+  int32_t reserved;
 };
 
 // Per-step scalars (host: binary64, rounded once) and the tensor table.
@@ -58,6 +86,10 @@ struct StepArgs {
   // betas, 1 - betas and gradient scale
   int32_t zero_ratio;
   uint32_t* tw_acc;
+  int32_t nsm;             // SMs of the device (persistent grids sized in the launcher)
+  int32_t stall_test;      // test hook: one warp withholds a copy so that its wait runs out
+  uint64_t wait_ns;        // bound of every wait for an async copy
+  uint32_t* status;        // the library's device status word (kStatus* bits are or-ed in)
   DevTensor t[kMaxTensors];
 };
 

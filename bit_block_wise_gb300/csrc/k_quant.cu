@@ -182,19 +182,12 @@ __global__ void k_fill(float* out, int n, float v) {
 
 cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s) {
   constexpr int bytes = QuantSmem::kBytes;
-  static unsigned configured[3] = {0u, 0u, 0u};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned bit = 1u << (dev & 31);
+  static std::atomic<unsigned char> configured[3][kMaxDevices];
   const void* fn = dtype == DT_F32 ? reinterpret_cast<const void*>(k_quantize<DT_F32>)
                    : dtype == DT_BF16 ? reinterpret_cast<const void*>(k_quantize<DT_BF16>)
                                       : reinterpret_cast<const void*>(k_quantize<DT_F16>);
-  if (!(configured[dtype] & bit)) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    configured[dtype] |= bit;
-  }
+  const cudaError_t e = set_smem_limit_once(fn, bytes, configured[dtype]);
+  if (e != cudaSuccess) return e;
   if (dtype == DT_F32) k_quantize<DT_F32><<<grid, kThreads, bytes, s>>>(a);
   else if (dtype == DT_BF16) k_quantize<DT_BF16><<<grid, kThreads, bytes, s>>>(a);
   else k_quantize<DT_F16><<<grid, kThreads, bytes, s>>>(a);

@@ -15,6 +15,7 @@
 #pragma once
 
 #include "bnb8_device.cuh"
+#include "k_step8_ring.cuh"
 
 namespace bnb8 {
 
@@ -525,23 +526,21 @@ cudaError_t launch_tw_store_t(const StepArgs& a, cudaStream_t s) {
 template <int OPT, int DT, int MODE, bool SKIP>
 cudaError_t launch_step8_skip(const StepArgs& a, int grid, cudaStream_t s) {
   constexpr int bytes = Step8Smem<OPT, MODE>::kBytes;
-  static unsigned configured = 0u;  // one bit per device: the attribute is per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned char> configured[kMaxDevices];  // the attribute is per device
+  const cudaError_t e = set_smem_limit_once(
+      reinterpret_cast<const void*>(k_step8<OPT, DT, MODE, SKIP>), bytes, configured);
   if (e != cudaSuccess) return e;
-  const unsigned bit = 1u << (dev & 31);
-  if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(k_step8<OPT, DT, MODE, SKIP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
   k_step8<OPT, DT, MODE, SKIP><<<grid, kThreads, bytes, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int OPT, int DT, int MODE>
 cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
+  // the plain step over blocks of 256 elements or more: the async-copy ring
+  // (AdEMAMix's three code streams do not fit its register budget yet)
+  if constexpr (OPT != ADEMAMIX && MODE == MODE_STEP) {
+    if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0) return launch_step8_ring<OPT, DT>(a, s);
+  }
   return a.skip_zeros ? launch_step8_skip<OPT, DT, MODE, true>(a, grid, s)
                       : launch_step8_skip<OPT, DT, MODE, false>(a, grid, s);
 }

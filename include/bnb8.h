@@ -88,9 +88,8 @@ enum bnb8_optim {
  *   state_bits  8 (block-wise dynamic quantization) or 32 (binary32 states;
  *            the docs page's min_8bit_size rule keeps tensors below 4096
  *            elements at 32 bits -- the caller picks per tensor).
- * Zero states: codes equal to the code of 0.0 in their map (127 for the
- * signed map, 0 for the unsigned map of bnb8_create_qmap) with absmax 0, or
- * binary32 zeros.
+ * Zero states: codes equal to the code of 0.0 in their map
+ * (bnb8_qmap_code(qmap, 0.0f, &code)) with absmax 0, or binary32 zeros.
  * Alignment: any element alignment is accepted; p/g/state arrays aligned to
  * 16 bytes (codes: 8 bytes, AdEMAMix needs n % 8 == 0 for the m2 half) take
  * the vectorised path. */
@@ -133,6 +132,7 @@ typedef struct bnb8_tensor {
  *               max_unorm * ||p of the block|| is scaled down to it.  The
  *               norms are formed inside the step (no pre-pass, no workspace);
  *               the multiplier matches the binary64 definition to 1e-6.
+ *               BNB8_TEST_STALL_WAIT: see enum bnb8_flags.
  *               Other bits: BNB8_EINVAL.
  *   step        1-based number of this update (bias corrections, schedules). */
 typedef struct bnb8_hparams {
@@ -141,18 +141,41 @@ typedef struct bnb8_hparams {
   int32_t blocksize;
   int32_t skip_zeros;
   float lr, beta1, beta2, beta3, alpha, eps, weight_decay, gnorm_scale, max_unorm;
-  int32_t flags; /* 0 or BNB8_UNORM_PER_BLOCK */
+  int32_t flags; /* 0, BNB8_UNORM_PER_BLOCK, BNB8_TEST_STALL_WAIT */
   int64_t step;
   int64_t t_alpha;
   int64_t t_beta3;
 } bnb8_hparams;
 
 enum bnb8_flags {
-  BNB8_UNORM_PER_BLOCK = 1 /* max_unorm per block instead of per tensor */
+  BNB8_UNORM_PER_BLOCK = 1, /* max_unorm per block instead of per tensor */
+  /* Test hook of the bounded waits (not for training): in a plain step
+   * (no skip_zeros, blocksize >= 256, max_unorm off or per tensor) one warp
+   * of the step kernel withholds one of its own asynchronous copies, so its
+   * wait for that copy runs out after 1 s.  The kernel then records
+   * BNB8_STATUS_WAIT_TIMEOUT in the device status (bnb8_device_status) and
+   * returns normally; the blocks of that warp are left partly or wholly
+   * unstepped.  No other flag bit is defined. */
+  BNB8_TEST_STALL_WAIT = 0x100
 };
 
 /* Message describing the last failure on this thread ("" if none). */
 const char* bnb8_last_error(void);
+
+/* Bits of the device status word. */
+enum bnb8_device_status_bits {
+  /* a step kernel's bounded wait for one of its asynchronous copies ran out
+   * (1 s); the call's results are incomplete */
+  BNB8_STATUS_WAIT_TIMEOUT = 1
+};
+
+/* The library keeps one 32-bit status word per device (a variable of the
+ * library's device code): the step kernels or-in enum bnb8_device_status_bits
+ * when a device-side wait gives up, instead of hanging or trapping.  This
+ * call copies the current device's word to *status (host), after the device
+ * has finished its work (it synchronizes the device), and zeroes the word if
+ * clear is nonzero.  Errors: BNB8_EINVAL (status NULL), BNB8_ECUDA. */
+int bnb8_device_status(uint32_t* status, int clear);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int bnb8_version(void);
@@ -166,6 +189,20 @@ int bnb8_version(void);
  * f = 7-k, plus 0 and +1.0.  Formed in binary64, rounded once.
  * Returns BNB8_EINVAL if out is NULL. */
 int bnb8_create_qmap(int is_signed, float* out);
+
+/* The code the nearest-level rule of block-wise quantization gives a
+ * normalised value x under a map (host): the number of map midpoints
+ * fl((qmap[j] + qmap[j+1]) * 0.5), j = 0..254, strictly below x (the nearest
+ * level, ties to the lower one) -- the rule bnb8_quantize_blockwise and the
+ * step functions apply to every value ("8-bit Optimizers via Block-wise
+ * Quantization", abstract: a value is stored as the index of its level in the
+ * dynamic data type).  Its use is the initial state: an all-zero state is
+ * the code of 0.0 in every element, for whatever map the caller steps with.
+ *   qmap   256 binary32 values, strictly ascending (host memory).
+ *   x      the value; code receives its code.
+ * Errors: BNB8_EINVAL if qmap or code is NULL, x is NaN, or qmap is not
+ * strictly ascending. */
+int bnb8_qmap_code(const float* qmap, float x, uint8_t* code);
 
 /* Block-wise quantization (device): for each block of B elements of x,
  * absmax[b] = max |x| over the block and codes[i] = the number of map

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 16
     assert sorted(bnb8.EXPORTS) == names
     for name in names:
         assert hasattr(L, name), name
@@ -54,6 +54,45 @@ def test_create_qmap_matches_oracle(L, signed):
 def test_create_qmap_null(L):
     assert L.bnb8_create_qmap(1, None) == bnb8.BNB8_EINVAL
     assert b"NULL" in L.bnb8_last_error()
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_qmap_code_matches_oracle_rule(L, signed):
+    q = oracle.create_qmap(signed)
+    mid = oracle.midpoints(q)
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([q, mid, np.nextafter(mid, np.float32(2)), np.nextafter(mid, np.float32(-2)),
+                         rng.uniform(-1.0, 1.0, 200).astype(np.float32), [0.0, -0.0, 2.0, -2.0]])
+    for x in xs.astype(np.float32):
+        assert bnb8.bnb8_qmap_code(q, float(x)) == oracle.code(mid, float(x)), x
+
+
+def test_zero_state_codes_come_from_the_map(L):
+    import torch
+    p = torch.zeros(1000)
+    s1, s2, a1, a2 = bnb8.zero_state(p, "adam", 8, 256)
+    S, U = oracle.create_qmap(True), oracle.create_qmap(False)
+    assert int(s1[0]) == int(np.count_nonzero(oracle.midpoints(S) < 0))
+    assert int(s2[0]) == int(np.count_nonzero(oracle.midpoints(U) < 0))
+    # a caller's map whose 0.0 sits at index 40: its zero state holds code 40
+    custom = np.concatenate([np.linspace(-1.0, -0.01, 40), [0.0],
+                             np.linspace(0.005, 1.0, 215)]).astype(np.float32)
+    assert np.all(np.diff(custom) > 0) and custom.size == 256
+    s1, s2, _, _ = bnb8.zero_state(p, "adam", 8, 256, qmap1=torch.from_numpy(custom))
+    assert torch.all(s1 == 40) and torch.all(s2 == int(s2[0])) and int(s2[0]) == 0
+    s1, _, _, _ = bnb8.zero_state(p, "rmsprop", 8, 256, qmap1=torch.from_numpy(custom))
+    assert torch.all(s1 == 40)
+
+
+def test_qmap_code_rejects_bad_maps(L):
+    q = oracle.create_qmap(True)
+    out = ctypes.c_uint8()
+    assert L.bnb8_qmap_code(None, 0.0, ctypes.byref(out)) == bnb8.BNB8_EINVAL
+    assert L.bnb8_qmap_code(q.ctypes.data, float("nan"), ctypes.byref(out)) == bnb8.BNB8_EINVAL
+    bad = q.copy()
+    bad[100] = bad[99]
+    assert L.bnb8_qmap_code(bad.ctypes.data, 0.0, ctypes.byref(out)) == bnb8.BNB8_EINVAL
+    assert b"ascending" in L.bnb8_last_error()
 
 
 def _hp(**kw):
