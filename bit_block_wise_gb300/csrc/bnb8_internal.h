@@ -88,6 +88,9 @@ struct StepArgs {
   uint32_t* tw_acc;
   int32_t nsm;             // SMs of the device (persistent grids sized in the launcher)
   int32_t stall_test;      // test hook: one warp withholds a copy so that its wait runs out
+  // 1 if every tensor of the launch has vec_ok == 3 and n a multiple of
+  // max(256, B): all its 256-element chunks are whole and bulk-copyable
+  int32_t whole;
   uint64_t wait_ns;        // bound of every wait for an async copy
   uint32_t* status;        // the library's device status word (kStatus* bits are or-ed in)
   DevTensor t[kMaxTensors];

@@ -159,12 +159,14 @@ __device__ __forceinline__ void cursor_settle(const StepArgs& a, ChunkCursor& c)
     ++c.t;
   }
 }
+// WHOLE: every chunk of the launch is whole (the host checked it).
+template <bool WHOLE>
 __device__ __forceinline__ ChunkRef cursor_chunk(const StepArgs& a, const ChunkCursor& c, int j) {
   ChunkRef r;
   r.t = c.t;
   r.lb = c.lb;
   r.e0 = (static_cast<int64_t>(c.lb) << a.log2B) + j * 256;
-  if (c.lb + 1 < tensor_blocks(a, c.t)) {
+  if (WHOLE || c.lb + 1 < tensor_blocks(a, c.t)) {
     r.v = 256;  // every block but a tensor's last is whole
   } else {
     const int64_t left = a.t[c.t].n - r.e0;
@@ -315,7 +317,11 @@ __device__ __forceinline__ void ring_group_max(uint32_t (&v)[NS], int G, int war
   }
 }
 
-template <int OPT, int DT>
+// WHOLE: every tensor of the launch is aligned for bulk copies and a
+// multiple of max(256, B) elements, so every chunk is whole and streams
+// through the ring; the element-wise paths for ragged or misaligned chunks are
+// compiled out.
+template <int OPT, int DT, bool WHOLE>
 __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_constant__ StepArgs a) {
   using L = RingSmem<OPT, DT>;
   constexpr int NS = L::NS;
@@ -382,9 +388,9 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
   for (int s = 0; s < kRingStages; ++s) {
     const int32_t b = b0 + s * NG;
     if (b < TB) {
-      const ChunkRef c = cursor_chunk(a, cur, j);
+      const ChunkRef c = cursor_chunk<WHOLE>(a, cur, j);
       put_header(c, s);
-      if (c.v == 256 && (a.t[c.t].vec_ok & 2)) {
+      if (WHOLE || (c.v == 256 && (a.t[c.t].vec_ok & 2))) {
         // the stall test withholds this warp's first copy: its wait must run out
         const bool withhold = stall_test && s == 0;
         if (lane == 0 && !withhold) issue(c, s);
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
 
     float p[8], g[8];
     uint2 cw[NS];
-    bool have = c.v > 0 && ok;
+    bool have = (WHOLE || c.v > 0) && ok;
     if ((want >> s) & 1u) {
       if (ok) {
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, (phase >> s) & 1u, a.wait_ns));
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
 #pragma unroll
         for (int k = 0; k < NS; ++k) am[k] = reinterpret_cast<const float*>(st + L::kSA)[k];
       }
-    } else if (have) {
+    } else if (!WHOLE && have) {
 #pragma unroll
       for (int k = 0; k < NS; ++k) am[k] = absmax_stream<OPT>(d, k, nb)[lb];
       global_load8<DT>(d.p, c.e0, c.v, lane, p);
@@ -464,10 +470,10 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
     if (ok) {
       const int32_t bn = b + kRingStages * NG;
       if (bn < TB) {
-        const ChunkRef cn = cursor_chunk(a, cur, j);
+        const ChunkRef cn = cursor_chunk<WHOLE>(a, cur, j);
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         put_header(cn, s);
-        if (cn.v == 256 && (a.t[cn.t].vec_ok & 2)) {
+        if (WHOLE || (cn.v == 256 && (a.t[cn.t].vec_ok & 2))) {
           if (lane == 0) issue(cn, s);
           want |= 1u << s;
           inflight |= 1u << s;
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
         }
       }
       // absent elements of a partial chunk keep state 0 (they do not count in the absmax)
-      if (c.v < 256) {
+      if (!WHOLE && c.v < 256) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int o = quad_offset<DT>(lane, q);
@@ -598,7 +604,7 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
           }
         }
       }
-      ring_store8<DT>(d.p, c.e0, c.v, (d.vec_ok & 1) != 0, lane, p);
+      ring_store8<DT>(d.p, c.e0, WHOLE ? 256 : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, p);
     } else {
 #pragma unroll
       for (int k = 0; k < NS; ++k)
@@ -612,38 +618,51 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
     if (!have) continue;
 
     // ---- requantize and store codes (and, once per block, the absmax) ----
-    float inv[NS];
-    bool all_fast = true;
+    // The usual case: every state's absmax lies in [2^-125, 2^125] (or is 0,
+    // an all-zero block) and every map takes the table: one Newton
+    // reciprocal per state and the table lookups, no other tests.
+    uint32_t enc[NS][8];
+    bool usual = true;
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
       const int m = Traits<OPT>::map_of(k);
-      const float amk = __uint_as_float(mx[k]);
-      inv[k] = rcp_block(amk);
-      all_fast = all_fast && fast_map[m] && mx[k] <= 0x7f7fffffu && inv[k] <= FLT_MAX &&
-                 (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
+      usual = usual && fast_map[m] && (mx[k] - 0x01000000u <= 0x7D000000u || mx[k] == 0u) &&
+              (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
     }
-    uint32_t enc[NS][8];
-    if (all_fast) {
+    if (usual) {
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
+        const float amk = __uint_as_float(mx[k]);
+        const float y = rcp_approx(amk);
+        const float r = __fmaf_rn(__fmaf_rn(-amk, y, 1.0f), y, y);
+        const float inv = mx[k] == 0u ? 0.0f : r;
         const uint32_t* tz = stbl + Traits<OPT>::map_of(k) * kTblSize + kTblZero;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          enc[k][e] = Traits<OPT>::nonneg(k) ? encode_fast_nonneg(sv[k][e], inv[k], tz)
-                                             : encode_fast(sv[k][e], inv[k], tz);
+        for (int e = 0; e < 8; e += 2) {
+          const float2 xn = mul2(make_float2(sv[k][e], sv[k][e + 1]), f2(inv));
+          if (Traits<OPT>::nonneg(k)) {
+            enc[k][e] = encode_xn_nonneg(xn.x, tz);
+            enc[k][e + 1] = encode_xn_nonneg(xn.y, tz);
+          } else {
+            enc[k][e] = encode_xn(xn.x, tz);
+            enc[k][e + 1] = encode_xn(xn.y, tz);
+          }
+        }
       }
     } else {
+      // absmax tiny, huge or not finite, or a map the table cannot take
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         const int m = Traits<OPT>::map_of(k);
-        const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv[k] <= FLT_MAX;
+        const float inv = rcp_block(__uint_as_float(mx[k]));
+        const bool fast = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
         const uint32_t* tz = stbl + m * kTblSize + kTblZero;
         const float* md = smid + m * 256;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          if (!fast) enc[k][e] = encode_search(sv[k][e] * inv[k], md);
-          else if (Traits<OPT>::nonneg(k) && nonneg_map[m]) enc[k][e] = encode_fast_nonneg(sv[k][e], inv[k], tz);
-          else enc[k][e] = encode_fast(sv[k][e], inv[k], tz);
+          if (!fast) enc[k][e] = encode_search(sv[k][e] * inv, md);
+          else if (Traits<OPT>::nonneg(k) && nonneg_map[m]) enc[k][e] = encode_fast_nonneg(sv[k][e], inv, tz);
+          else enc[k][e] = encode_fast(sv[k][e], inv, tz);
         }
       }
     }
@@ -654,8 +673,8 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
                                       __byte_perm(enc[k][2], enc[k][3], 0x0062u), 0x5410u);
       const uint32_t hi = __byte_perm(__byte_perm(enc[k][4], enc[k][5], 0x0062u),
                                       __byte_perm(enc[k][6], enc[k][7], 0x0062u), 0x5410u);
-      ring_store_codes<DT>(const_cast<uint8_t*>(code_stream<OPT>(d, k)), c.e0, c.v,
-                           (d.vec_ok & 1) != 0, lane, make_uint2(lo, hi));
+      ring_store_codes<DT>(const_cast<uint8_t*>(code_stream<OPT>(d, k)), c.e0, WHOLE ? 256 : c.v,
+                           WHOLE || (d.vec_ok & 1) != 0, lane, make_uint2(lo, hi));
       if (j == 0 && lane == 0) absmax_stream<OPT>(d, k, nb)[lb] = __uint_as_float(mx[k]);
     }
   }
@@ -677,11 +696,11 @@ __host__ __forceinline__ int ring_threads(int log2B) {
   return groups * G * 32;
 }
 
-template <int OPT, int DT>
-cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
+template <int OPT, int DT, bool WHOLE>
+cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   using L = RingSmem<OPT, DT>;
   static std::atomic<unsigned char> configured[kMaxDevices];
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT>),
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE>),
                                       L::kBytes, configured);
   if (e != cudaSuccess) return e;
   const int threads = ring_threads<OPT, DT>(a.log2B);
@@ -689,8 +708,13 @@ cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
   const int64_t groups = threads / 32 / G;
   const int64_t need = (a.total_blocks + groups - 1) / groups;
   const int grid = static_cast<int>(need < a.nsm ? need : a.nsm);
-  k_step8_ring<OPT, DT><<<grid, threads, L::kBytes, s>>>(a);
+  k_step8_ring<OPT, DT, WHOLE><<<grid, threads, L::kBytes, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int OPT, int DT>
+cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
+  return a.whole ? launch_step8_ring_w<OPT, DT, true>(a, s) : launch_step8_ring_w<OPT, DT, false>(a, s);
 }
 
 }  // namespace bnb8
