@@ -60,10 +60,16 @@ class Workload:
     the timed region), so that each timed step migrates them back."""
 
     def __init__(self, name, desc, optim, dtype, sizes, bits, blocksize, hp, grad, p_std=0.02,
-                 op="step", paged=None):
+                 op="step", paged=None, carry=False):
         self.name, self.desc, self.optim, self.dtype = name, desc, optim, dtype
         self.sizes, self.bits, self.blocksize, self.hp = sizes, bits, blocksize, hp
         self.grad, self.p_std, self.op, self.paged = grad, p_std, op, paged
+        self.carry = carry   # ||p|| carried between steps (BNB8_CARRY_PNORM)
+
+    def lib_hp(self):
+        """Keyword arguments of the library's HParams (the oracle's plus the
+        carried-norm switch, which changes no result's definition)."""
+        return dict(self.hp, carry_pnorm=self.carry)
 
     @property
     def elements(self):
@@ -92,8 +98,13 @@ class Workload:
                 rest = n * (2 * e + 8 * ns)                # p r+w, binary32 states r+w
             total += n * e + rest * live_block_frac        # g always read
             if self.hp.get("max_unorm", 0.0) > 0 and not self.hp.get("unorm_per_block"):
-                # the per-tensor pre-pass reads g, p, states (per block: inside the step)
-                total += n * 2 * e + (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
+                # the per-tensor pre-pass reads g, p, states (per block: inside
+                # the step); with the norm carried from the previous step it
+                # reads p only when the direction needs it (coupled decay)
+                decoupled = self.optim in ("adamw", "lion", "ademamix")
+                p_read = not (self.carry and (decoupled or self.hp.get("weight_decay", 0.0) == 0))
+                total += n * e * (2 if p_read else 1) + \
+                    (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
         return int(total)
 
 
@@ -168,16 +179,18 @@ def _cfg_paged(mode):
         ("outliers", 1e-3, 1e-1, 0.01), paged=mode)
 
 
-def _cfg_gpt2xl():
+def _cfg_gpt2xl(optim="adam", carry=False):
     shapes = workloads.gpt2_xl_params()
     sizes = [n for _, n in shapes]
     bits = [8 if n >= 4096 else 32 for n in sizes]
-    return Workload("gpt2xl_list_bf16_adam8bit_B256_maxunorm1",
+    name = "Adam" if optim == "adam" else "AdamW"
+    return Workload(f"gpt2xl_list_bf16_{optim}8bit_B256_maxunorm1{'_carried' if carry else ''}",
                     "GPT-2-XL-shaped list (580 tensors, 1,557,611,200 elements), bf16 p/g, "
-                    "tensors < 4096 elements at 32-bit state, Adam8bit B256, max_unorm 1.0, wd 0.1",
-                    "adam", "bf16", sizes, bits, 256,
+                    f"tensors < 4096 elements at 32-bit state, {name}8bit B256, max_unorm 1.0, "
+                    f"wd 0.1{', ||p|| carried from the previous step' if carry else ''}",
+                    optim, "bf16", sizes, bits, 256,
                     dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1,
-                         max_unorm=1.0), ("normal", 1e-3))
+                         max_unorm=1.0), ("normal", 1e-3), carry=carry)
 
 
 WORKLOADS = {
@@ -208,6 +221,9 @@ WORKLOADS = {
                                           alpha=5.0, t_alpha=100, t_beta3=100, eps=1e-8),
                                      ("normal", 1e-3)),
     "gpt2xl": _cfg_gpt2xl,
+    "gpt2xl_carried": lambda: _cfg_gpt2xl("adam", True),
+    "gpt2xl_adamw": lambda: _cfg_gpt2xl("adamw"),
+    "gpt2xl_adamw_carried": lambda: _cfg_gpt2xl("adamw", True),
     **{f"{o}_embedding{sfx}": (lambda o=o, sk=sk: _cfg_embedding(o, sk))
        for o in ("momentum", "rmsprop", "adagrad", "lion", "adam") for sfx, sk in (("", True), ("_noskip", False))
        if not (o == "momentum" and sk)},
@@ -449,7 +465,7 @@ def run_gpu(args, wl):
 
     # the library's marshal-once entry (Stepper), one per gradient set of the
     # pool: inside the timed region a step is one ctypes call
-    hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **hp_kw)
+    hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **wl.lib_hp())
     steppers = []
     for k in range(pool):
         for ps, g in zip(params, grads[k]):
@@ -544,7 +560,12 @@ def run_gpu(args, wl):
             "state_bytes": int(sum(t.numel() * t.element_size() for t in state_arrays)),
             "migrated_host_to_device_in_timed_step": wl.paged == "evicted"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the CPU (oracle) leg: the timed baseline, then the oracle's check of
+        # one more GPU step on sampled blocks (outside every timed region)
         out["cpu_baseline"] = cpu_baseline(wl, params, budget_s=args.cpu_budget)
+        step_no[0] += 1
+        out["parity_sample"] = sampled_parity(
+            wl, params, lambda: steppers[0](step_no[0], stream), step_no[0], grads[0])
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -615,16 +636,27 @@ def run_e2e(args, wl, bnb8, params, q1, q2, workspace, ws_bytes, stream, step_no
     host_p = [torch.empty(n, dtype=tdt, pin_memory=True) for n in wl.sizes]
     for hg, ps in zip(host_g, params):
         hg.copy_(ps.g if ps.g is not None else torch.zeros_like(ps.p))
-    hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **wl.hp)
+    hp0 = bnb8.HParams(optim=wl.optim, blocksize=wl.blocksize, step=1, **wl.lib_hp())
     dev_g, groups, steppers = [], [], []
+    # a carried norm lives in the workspace of its own tensor list: one per
+    # group, shared by the group's two gradient buffers
+    group_ws = {}
+
+    def ws_for(c):
+        if not ws_bytes:
+            return None
+        if not wl.carry:
+            return workspace
+        if c not in group_ws:
+            group_ws[c] = torch.zeros_like(workspace)
+        return group_ws[c]
     for buf in range(2):
         dev_g.append([torch.empty_like(ps.p) for ps in params])
         for ps, dg in zip(params, dev_g[buf]):
             ps.g = dg
         groups.append(e2e_groups(bnb8, params, wl, 4))
-        steppers.append([bnb8.Stepper([pc for _, _, pc in grp], hp0, q1, q2,
-                                      workspace=workspace if ws_bytes else None)
-                         for grp in groups[buf]])
+        steppers.append([bnb8.Stepper([pc for _, _, pc in grp], hp0, q1, q2, workspace=ws_for(c))
+                         for c, grp in enumerate(groups[buf])])
     ngroups = len(groups[0])
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_up = [torch.cuda.Event() for _ in range(ngroups)]
@@ -874,6 +906,88 @@ def time_oracle(wl, n_sample, steps, budget_s):
 def calibrate_oracle(wl):
     n, done, el = time_oracle(wl, 16 * _gran(wl), 2, 10.0)
     return el / done / n  # seconds per element
+
+
+def _host_bits(t):
+    """A device tensor as numpy: float32 as float32, 16-bit floats as their
+    uint16 patterns (the oracle's storage form), others as they are."""
+    import torch
+    t = t.detach().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def sampled_parity(wl, params, gpu_step, step, grads, nsample=48, seed=7):
+    """The oracle's check of one GPU step on sampled blocks of the first 8-bit
+    tensor: the blocks' p, g, codes and absmax are copied out, the GPU steps
+    the whole workload once, and the oracle steps the copies.  Reports the
+    share of code mismatches and their largest index distance (the method
+    allows at most one index, at exact ties), plus absmax and p mismatches
+    (p only where no per-tensor max_unorm multiplier enters, since that
+    needs the whole tensor)."""
+    import torch
+    import oracle
+    oracle.build()
+    idx = next((i for i, ps in enumerate(params) if ps.state_bits == 8), None)
+    B = wl.blocksize
+    if idx is None or B == 0:
+        return None
+    ps = params[idx]
+    n = ps.p.numel()
+    nb = -(-n // B)
+    rng = np.random.default_rng(seed)
+    blocks = sorted(set(rng.choice(nb, size=min(nsample, nb), replace=False).tolist()) | {0, nb - 1})
+    full = [b for b in blocks if (b + 1) * B <= n]
+    part = [b for b in blocks if (b + 1) * B > n]
+    two = ps.s1.numel() == 2 * n  # AdEMAMix: m1 and m2 stacked
+
+    def elems(group, base=0):
+        return torch.cat([torch.arange(base + b * B, base + min(n, (b + 1) * B), device=ps.p.device)
+                          for b in group])
+
+    def snapshot(group):
+        e = elems(group)
+        bi = torch.tensor(group, device=ps.p.device)
+        s1 = torch.cat([ps.s1[e], ps.s1[elems(group, n)]]) if two else ps.s1[e]
+        a1 = torch.cat([ps.absmax1[bi], ps.absmax1[bi + nb]]) if two else ps.absmax1[bi]
+        return oracle.TensorState(_host_bits(ps.p[e]), _host_bits(s1),
+                                  None if ps.s2 is None else _host_bits(ps.s2[e]), _host_bits(a1),
+                                  None if ps.absmax2 is None else _host_bits(ps.absmax2[bi]), 8)
+
+    before = [(g, snapshot(g), _host_bits(grads[idx][elems(g)])) for g in (full, part) if g]
+    gpu_step()
+    if ps.p.is_cuda:
+        torch.cuda.synchronize()
+    q1 = oracle.create_qmap(wl.optim not in ("rmsprop", "adagrad"))
+    q2 = oracle.create_qmap(False)
+    hp = oracle.HParams(optim=wl.optim, step=step, **wl.hp)
+    compare_p = not (wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block"))
+    codes = mism = maxd = am_bad = p_bad = p_total = 0
+    for group, ref, g in before:
+        got = snapshot(group)
+        oracle.step(hp, ref, g, wl.dtype, B, q1, q2)
+        for a, b in ((got.s1, ref.s1), (got.s2, ref.s2)):
+            if a is None:
+                continue
+            d = np.abs(a.astype(np.int32) - b.astype(np.int32))
+            codes += d.size
+            mism += int(np.count_nonzero(d))
+            maxd = max(maxd, int(d.max()) if d.size else 0)
+        for a, b in ((got.absmax1, ref.absmax1), (got.absmax2, ref.absmax2)):
+            if a is not None:
+                am_bad += int(np.count_nonzero(a.view(np.uint32) != b.view(np.uint32)))
+        if compare_p:
+            p_total += got.p.size
+            if got.p.size:
+                differ = (got.p.view(np.uint8).reshape(got.p.size, -1) !=
+                          ref.p.view(np.uint8).reshape(ref.p.size, -1))
+                p_bad += int(differ.any(axis=1).sum())
+    return {"kind": "oracle", "blocks": len(blocks), "codes": codes,
+            "code_mismatch_rate": mism / max(codes, 1), "code_mismatches": mism,
+            "code_mismatch_max_index_delta": maxd, "absmax_mismatches": am_bad,
+            "p_compared": p_total, "p_mismatches": p_bad if compare_p else None,
+            "step": step, "tensor": idx}
 
 
 def cpu_baseline(wl, params=None, budget_s=15.0):

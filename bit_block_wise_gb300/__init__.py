@@ -24,6 +24,7 @@ BNB8_OK, BNB8_EINVAL, BNB8_EUNSUPPORTED, BNB8_ECUDA, BNB8_EWORKSPACE = 0, 1, 2, 
 BNB8_F32, BNB8_BF16, BNB8_F16 = 0, 1, 2
 BNB8_ADAM, BNB8_ADAMW, BNB8_MOMENTUM, BNB8_RMSPROP, BNB8_ADAGRAD, BNB8_LION, BNB8_ADEMAMIX = range(7)
 BNB8_UNORM_PER_BLOCK = 1
+BNB8_CARRY_PNORM = 2
 BNB8_TEST_STALL_WAIT = 0x100
 BNB8_STATUS_WAIT_TIMEOUT = 1
 BNB8_PAGED_HOST = -1
@@ -160,10 +161,12 @@ class HParams:
     skip_zeros: bool = False
     blocksize: int = 256
     unorm_per_block: bool = False  # max_unorm per block (BNB8_UNORM_PER_BLOCK)
+    carry_pnorm: bool = False      # carry ||p|| to the next step (BNB8_CARRY_PNORM)
     extra_flags: int = 0           # other hparams.flags bits (BNB8_TEST_STALL_WAIT)
 
     def c(self, dtype_code: int) -> Bnb8Hparams:
-        flags = (BNB8_UNORM_PER_BLOCK if self.unorm_per_block else 0) | int(self.extra_flags)
+        flags = ((BNB8_UNORM_PER_BLOCK if self.unorm_per_block else 0) |
+                 (BNB8_CARRY_PNORM if self.carry_pnorm else 0) | int(self.extra_flags))
         return Bnb8Hparams(OPTIMS[self.optim], dtype_code, self.blocksize, int(bool(self.skip_zeros)),
                            self.lr, self.beta1, self.beta2, self.beta3, self.alpha, self.eps,
                            self.weight_decay, self.gnorm_scale, self.max_unorm, flags,
@@ -351,10 +354,11 @@ def bnb8_unorm(params, hp: HParams, qmap1, qmap2=None, out_scale=None, workspace
 def bnb8_unorm_static(params, hp: HParams, qmap1, qmap2=None, out_scale=None, stream=None):
     """bnb8_unorm without a workspace: for callers that cannot allocate device
     memory (the library's fixed 2 MiB scratch array holds the partial norms;
-    at most 262,144 blocks per call; calls that overlap on the GPU race)."""
-    torch = _torch()
+    at most 262,144 blocks per call; calls that overlap on the GPU race).
+    out_scale (a float32 device tensor of len(params)) is required: this
+    wrapper allocates nothing either."""
     if out_scale is None:
-        out_scale = torch.empty(len(params), dtype=torch.float32, device=params[0].p.device)
+        raise ValueError("bnb8_unorm_static needs out_scale: it allocates no device memory")
     arr = _tensor_array(params)
     hc = hp.c(_dtype_code(params[0].p))
     _check(lib().bnb8_unorm_static(arr, len(params), ctypes.byref(hc), _ptr(qmap1), _ptr(qmap2),

@@ -145,7 +145,7 @@ int check_hparams(const bnb8_hparams* hp, const int* allowed, int nallowed, int*
                 hp->blocksize);
   if (hp->blocksize == 0 && (hp->flags & BNB8_UNORM_PER_BLOCK) != 0)
     return fail(BNB8_EINVAL, "BNB8_UNORM_PER_BLOCK needs blocks (blocksize 0 is tensor-wise)");
-  const int known = BNB8_UNORM_PER_BLOCK | BNB8_TEST_STALL_WAIT;
+  const int known = BNB8_UNORM_PER_BLOCK | BNB8_CARRY_PNORM | BNB8_TEST_STALL_WAIT;
   if ((hp->flags & ~known) != 0)
     return fail(BNB8_EINVAL, "hparams.flags: unknown bits 0x%x", hp->flags & ~known);
   if (hp->step < 1) return fail(BNB8_EINVAL, "step must be >= 1 (got %lld)", (long long)hp->step);
@@ -290,12 +290,43 @@ int device_status_addr(uint32_t** out) {
 // Bound of every wait for an async copy inside the step kernels.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Workspace layout: [per-tensor max_unorm multipliers][per-block partials]
-// when the per-tensor pre-pass runs, then [4 words per tensor] of tensor-wise
-// absmax accumulators when blocksize is 0.
+// Workspace layout when the per-tensor pre-pass runs: [the carried norm's
+// stamp, in its own 256 bytes][per-tensor max_unorm multipliers][per-block
+// partials]; then [4 words per tensor] of tensor-wise absmax accumulators
+// when blocksize is 0.  The stamp sits at the same place for every tensor
+// list, so any call that reuses the workspace for another list replaces it.
+constexpr size_t kStampBytes = 256;
+size_t partials_offset(int nt) { return kStampBytes + align256(static_cast<size_t>(nt) * sizeof(float)); }
 size_t workspace_bytes_for(int nt, int64_t all_blocks) {
-  return align256(static_cast<size_t>(nt) * sizeof(float)) +
-         align256(static_cast<size_t>(all_blocks) * sizeof(float2));
+  return partials_offset(nt) + align256(static_cast<size_t>(all_blocks) * sizeof(float2));
+}
+
+// The carried norm's stamp: a hash of the tensor list and the settings that
+// shape its partials (FNV-1a over 64-bit words), mixed with a step number.
+uint64_t list_hash(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  auto mix = [&](uint64_t v) {
+    for (int i = 0; i < 8; ++i) {
+      h ^= (v >> (8 * i)) & 0xffu;
+      h *= 0x100000001b3ull;
+    }
+  };
+  mix(static_cast<uint64_t>(hp.optim));
+  mix(static_cast<uint64_t>(hp.dtype));
+  mix(static_cast<uint64_t>(hp.blocksize));
+  mix(static_cast<uint64_t>(nt));
+  for (int i = 0; i < nt; ++i) {
+    mix(reinterpret_cast<uintptr_t>(ts[i].p));
+    mix(static_cast<uint64_t>(ts[i].n));
+    mix(static_cast<uint64_t>(ts[i].state_bits));
+  }
+  return h;
+}
+uint64_t carry_stamp_for(uint64_t list, int64_t step) {
+  uint64_t z = list ^ (static_cast<uint64_t>(step) * 0x9e3779b97f4a7c15ull);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return (z ^ (z >> 31)) | 1ull;  // never 0, the contents of a cleared workspace
 }
 size_t tw_bytes_for(int nt) { return align256(static_cast<size_t>(nt) * 4 * sizeof(uint32_t)); }
 
@@ -382,12 +413,17 @@ int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int
 // max_unorm pre-pass + finalize into out_scale[caller index].
 int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparams& hp,
               const Scalars& sc, int log2B, const float* qmap1, const float* qmap2,
-              float* out_scale, float2* partials, cudaStream_t stream) {
+              float* out_scale, float2* partials, cudaStream_t stream,
+              uint64_t* stamp = nullptr, uint64_t carry_expect = 0) {
   cudaError_t e = launch_fill(out_scale, nt, 1.0f, stream);  // n == 0 tensors keep 1
   if (e != cudaSuccess) return cuda_fail(e, "unorm fill");
-  for (const Plan::Chunk& c : plan.chunks) {
+  for (size_t ci = 0; ci < plan.chunks.size(); ++ci) {
+    const Plan::Chunk& c = plan.chunks[ci];
     StepArgs a = make_args(c, ts, plan, hp, sc, log2B, qmap1, qmap2);
     a.partials = partials + c.partial_offset;
+    // carry_expect 0: no carried norm (a stamp is never 0)
+    a.carry_stamp = carry_expect != 0 ? stamp : nullptr;
+    a.carry_expect = carry_expect;
     const int grid = grid_for(c.bits, hp.optim, hp.dtype, MODE_NORM, c.total_blocks, log2B);
     e = launch_family(c.bits, hp.optim, hp.dtype, MODE_NORM, a, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "unorm pre-pass launch");
@@ -398,6 +434,9 @@ int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparam
     f.unorm_c = sc.unorm_c;
     f.max_unorm = hp.max_unorm;
     f.ntensors = a.ntensors;
+    // these partials no longer hold a carried norm: the last finalize clears
+    // the stamp (a step that carries the norm writes a new one after it)
+    f.stamp_clear = ci + 1 == plan.chunks.size() ? stamp : nullptr;
     int64_t chunks = 0;
     for (int k = 0; k < a.ntensors; ++k) {
       f.first_block[k] = a.t[k].first_block;
@@ -443,10 +482,18 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
   uint32_t* tw_acc = tw ? reinterpret_cast<uint32_t*>(
                               static_cast<char*>(ws) + (prepass ? workspace_bytes_for(nt, plan.all_blocks) : 0))
                         : nullptr;
+  float2* partials = nullptr;
+  uint64_t* stamp = nullptr;      // the carried norm's stamp (workspace offset 0)
+  // no carry with blocksize 0 (tensor-wise steps leave no per-block sums) or
+  // with skip_zeros (a skipped block reads no p, so it could not leave its sum)
+  const bool carry = prepass && !tw && hp->skip_zeros == 0 && (hp->flags & BNB8_CARRY_PNORM) != 0;
+  const uint64_t list = carry ? list_hash(ts, nt, *hp) : 0;
   if (prepass) {
-    float* scales = static_cast<float*>(ws);
-    float2* partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(nt * sizeof(float)));
-    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream);
+    float* scales = reinterpret_cast<float*>(static_cast<char*>(ws) + kStampBytes);
+    partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + partials_offset(nt));
+    stamp = static_cast<uint64_t*>(ws);
+    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream, stamp,
+                   carry ? carry_stamp_for(list, hp->step - 1) : 0);
     if (rc != BNB8_OK) return rc;
     clip = scales;
   }
@@ -464,11 +511,20 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
       if (e != cudaSuccess) return cuda_fail(e, "tensor-wise max launch");
     }
   }
-  for (const Plan::Chunk& c : plan.chunks) {
+  for (size_t ci = 0; ci < plan.chunks.size(); ++ci) {
+    const Plan::Chunk& c = plan.chunks[ci];
     StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
     a.clip = clip;
     a.tw_acc = tw_acc;
     a.status = status;
+    if (carry) {
+      // every launch leaves its blocks' sums of p^2; the last one stamps them
+      a.carry_out = 1;
+      a.partials = partials + c.partial_offset;
+      a.carry_stamp = stamp;
+      a.carry_writer = ci + 1 == plan.chunks.size() ? 1 : 0;
+      a.carry_write = carry_stamp_for(list, hp->step);
+    }
     const int m = (tw && c.bits == 8) ? MODE_TWSTEP : mode;
     const int grid = grid_for(c.bits, hp->optim, hp->dtype, m, c.total_blocks, log2B);
     const cudaError_t e = launch_family(c.bits, hp->optim, hp->dtype, m, a, grid, stream);
@@ -687,10 +743,10 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
     return fail(BNB8_EWORKSPACE, "unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
                 need, workspace_bytes);
-  float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                               align256(ntensors * sizeof(float)));
+  float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) + partials_offset(ntensors));
   const Scalars sc = make_scalars(*hp);
-  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s);
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s,
+                   static_cast<uint64_t*>(workspace));
 }
 
 }  // extern "C"

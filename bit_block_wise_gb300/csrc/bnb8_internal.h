@@ -93,6 +93,16 @@ struct StepArgs {
   int32_t whole;
   uint64_t wait_ns;        // bound of every wait for an async copy
   uint32_t* status;        // the library's device status word (kStatus* bits are or-ed in)
+  // The carried parameter norm (BNB8_CARRY_PNORM): a MODE_STEP launch with
+  // carry_out set leaves the sum of the new p^2 of each block in
+  // partials[block].y; the launch with carry_writer set then stores carry_write
+  // in *carry_stamp.  A MODE_NORM launch whose *carry_stamp equals
+  // carry_expect takes those sums instead of reading p for them.
+  int32_t carry_out;
+  int32_t carry_writer;
+  uint64_t* carry_stamp;
+  uint64_t carry_expect;
+  uint64_t carry_write;
   DevTensor t[kMaxTensors];
 };
 
@@ -131,6 +141,7 @@ struct FinalizeArgs {
   int64_t first_block[kMaxTensors + 1];
   int64_t first_chunk[kMaxTensors + 1];  // chunks of tensors 0..t-1
   int32_t index[kMaxTensors];
+  uint64_t* stamp_clear;   // set to 0 (the carried norm's stamp), or null
 };
 
 // Kernel launchers (defined in the kernel translation units).  Each returns

@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(256) k_unorm_finalize(const __grid_constant__ 
     const double limit = a.max_unorm * sqrt(sp[0]);
     a.out_scale[a.index[t]] = (a.max_unorm > 0.0 && unorm > limit) ? static_cast<float>(limit / unorm)
                                                                     : 1.0f;
+    if (t == 0 && a.stamp_clear != nullptr) *a.stamp_clear = 0ull;
   }
 }
 

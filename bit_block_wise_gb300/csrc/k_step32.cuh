@@ -25,6 +25,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
   const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
   int parity = 0;
+  // the pre-pass with a carried parameter norm (see k_step8)
+  const bool carried = MODE == MODE_NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
+  const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));
 
   for (int64_t base = warp_g0; base < a.total_blocks; base += stride) {
     const int64_t gb = base + in_warp;
@@ -41,7 +44,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
                     static_cast<float*>(d.s2)};
 
     float p[8], g[8], s[NS][8];
-    load8<DT, false>(d.p, e0, valid, vec, p);
+    if (MODE != MODE_NORM || read_p) {
+      load8<DT, false>(d.p, e0, valid, vec, p);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) p[j] = 0.0f;
+    }
     load8<DT, true>(d.g, e0, valid, vec, g);
 #pragma unroll
     for (int k = 0; k < NS; ++k) load8<DT_F32, false>(sp[k], e0, valid, vec, s[k]);
@@ -76,7 +84,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
       float r[2] = {usq, psq};
       group_reduce<2, false>(r, GT, glocal, sred, parity);
       parity ^= 1;
-      if (active && gtid == 0) a.partials[gb] = make_float2(r[0], r[1]);
+      if (active && gtid == 0) {
+        if (carried) a.partials[gb].x = r[0];
+        else a.partials[gb] = make_float2(r[0], r[1]);
+      }
       continue;
     }
     if constexpr (MODE == MODE_BCLIP) {
@@ -91,11 +102,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
       for (int j = 0; j < 8; ++j)
         if (!((held >> j) & 1u)) elem_apply<OPT>(a, eff_b, p[j], ud[j]);
     }
+    if (MODE == MODE_STEP && a.carry_out) {
+      // the block's sum of the new p^2 as stored, for the next step's max_unorm
+      float r[1] = {0.0f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float q = Elem<DT>::stored(p[j]);
+        if (j < valid) r[0] = r[0] + q * q;
+      }
+      group_reduce<1, false>(r, GT, glocal, sred, parity);
+      parity ^= 1;
+      if (active && gtid == 0) a.partials[gb].y = r[0];
+    }
     if (!any) continue;  // every element skipped: leave them untouched
     store8<DT>(d.p, e0, valid, vec, p);
 #pragma unroll
     for (int k = 0; k < NS; ++k) store8<DT_F32>(sp[k], e0, valid, vec, s[k]);
   }
+  if (MODE == MODE_STEP && a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0)
+    *a.carry_stamp = a.carry_write;
 }
 
 template <int OPT, int DT, int MODE>

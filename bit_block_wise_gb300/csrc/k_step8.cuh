@@ -168,6 +168,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   __shared__ int s_scan[2 * 32];
 
   const int tid = threadIdx.x;
+  // the pre-pass with a carried parameter norm (BNB8_CARRY_PNORM): the sums
+  // of p^2 are already in the partials; p is not read when the direction does
+  // not depend on it
+  const bool carried = MODE == MODE_NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
+  const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));
   // ---- stage the maps, midpoints and (step mode) the bucket tables ----
   for (int i = tid; i < NM * 256; i += kThreads) sq[i] = i < 256 ? a.qmap1[i] : a.qmap2[i - 256];
   if (tid < 2) s_bad[tid] = 0;
@@ -287,7 +292,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         if (!group_nz && !tw) continue;
         load8<DT, false>(d.p, e0, valid, vec, p);
       } else {
-        load8<DT, false>(d.p, e0, valid, vec, p);
+        if (MODE != MODE_NORM || read_p) {
+          load8<DT, false>(d.p, e0, valid, vec, p);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p[e] = 0.0f;
+        }
         load8<DT, true>(d.g, e0, valid, vec, g);
       }
 #pragma unroll
@@ -408,7 +418,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
         float r[2] = {usq, psq};
         group_reduce<2, false>(r, GT, glocal, sred, parity);
         parity ^= 1;
-        if (active && gtid == 0) a.partials[fb + blk] = make_float2(r[0], r[1]);
+        if (active && gtid == 0) {
+          if (carried) a.partials[fb + blk].x = r[0];
+          else a.partials[fb + blk] = make_float2(r[0], r[1]);
+        }
         continue;
       }
       if constexpr (MODE == MODE_TWMAX) {
@@ -441,6 +454,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       // only when skip_zeros could not leave its warp early, with the same
       // bits)
       if (active && any) store8<DT>(d.p, e0, valid, vec, p);
+      if (MODE == MODE_STEP && a.carry_out) {
+        // the block's sum of the new p^2 as stored (skipped elements keep theirs)
+        float r[1] = {0.0f};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float q = Elem<DT>::stored(p[e]);
+          if (e < valid) r[0] = r[0] + q * q;
+        }
+        group_reduce<1, false>(r, GT, glocal, sred, parity);
+        parity ^= 1;
+        if (active && gtid == 0) a.partials[fb + blk].y = r[0];
+      }
       if (kAheadAm) {
         // the next block of this tensor, when all 8 of this thread's elements
         // exist there and its streams are aligned (else it loads as usual)
@@ -500,6 +525,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
       __syncthreads();
     }
   }
+  if (MODE == MODE_STEP && a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0)
+    *a.carry_stamp = a.carry_write;
 }
 
 // Tensor-wise quantization: after the step, the new absmax of each updated

@@ -321,6 +321,24 @@ __device__ __forceinline__ void ring_group_max(uint32_t (&v)[NS], int G, int war
 // multiple of max(256, B) elements, so every chunk is whole and streams
 // through the ring; the element-wise paths for ragged or misaligned chunks are
 // compiled out.
+// Sum of v over the G warps of a group, in a fixed order (as ring_group_max).
+__device__ __forceinline__ float ring_group_sum(float v, int G, int warp, int lane, uint32_t* red,
+                                                int parity) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (G > 1) {
+    float* slot = reinterpret_cast<float*>(red + parity * 32 * 4);
+    if (lane == 0) slot[warp * 4] = v;
+    const int grp = warp / G;
+    named_barrier(1 + grp, G * 32);
+    const int w0 = grp * G;
+    float acc = slot[w0 * 4];
+    for (int w = 1; w < G; ++w) acc += slot[(w0 + w) * 4];
+    v = acc;
+  }
+  return v;
+}
+
 template <int OPT, int DT, bool WHOLE>
 __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_constant__ StepArgs a) {
   using L = RingSmem<OPT, DT>;
@@ -486,6 +504,7 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
     // ---- dequantize and update; new states in sv, running max of |s| in mx ----
     float sv[NS][8];
     uint32_t mx[NS];
+    float psq = 0.0f;        // sum of the new p^2 (the carried norm)
 #pragma unroll
     for (int k = 0; k < NS; ++k) mx[k] = 0u;
     const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
@@ -605,6 +624,15 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
         }
       }
       ring_store8<DT>(d.p, c.e0, WHOLE ? 256 : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, p);
+      if (a.carry_out) {
+        // the squares of p as stored (rounded to the dtype); the registers
+        // of a ragged chunk's absent elements hold no parameter
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float q = Elem<DT>::stored(p[e]);
+          if (WHOLE || quad_offset<DT>(lane, e >> 2) + (e & 3) < c.v) psq = psq + q * q;
+        }
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < NS; ++k)
@@ -615,6 +643,12 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
     // ---- the block's new absmax (every warp of the group takes part) ----
     ring_group_max<NS>(mx, G, warp, lane, sred, parity);
     parity ^= 1;
+    if (a.carry_out) {
+      const float bsq = ring_group_sum(psq, G, warp, lane, sred, parity);
+      parity ^= 1;
+      if (have && j == 0 && lane == 0)
+        reinterpret_cast<float*>(a.partials + d.first_block + lb)[1] = bsq;
+    }
     if (!have) continue;
 
     // ---- requantize and store codes (and, once per block, the absmax) ----
@@ -678,6 +712,8 @@ __global__ void __launch_bounds__(kRingWarps * 32, 1) k_step8_ring(const __grid_
       if (j == 0 && lane == 0) absmax_stream<OPT>(d, k, nb)[lb] = __uint_as_float(mx[k]);
     }
   }
+
+  if (a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0) *a.carry_stamp = a.carry_write;
 
   // ---- a wait ran out: let this warp's copies still in flight land ----
   if (!ok && lane == 0) {

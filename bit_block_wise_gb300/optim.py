@@ -21,13 +21,19 @@ parameters it updates to their device, on the step's stream: one call per
 buffer, whose pages the step then finds resident instead of faulting them in
 (several times slower).  page_prefetch=False leaves placement to the driver:
 no per-step call, which saves its cost when the states stay resident.
+
+carry_pnorm=True (with max_unorm per tensor): each batch keeps its workspace
+from step to step, and the library carries ||p|| from one step to the next
+(hparams flag BNB8_CARRY_PNORM) instead of reading p again for it.  The
+parameters must then change only through this optimizer between steps;
+load_state_dict() and invalidate_carried_norms() drop the carried norms.
 """
 from __future__ import annotations
 
 import torch
 
-from . import HParams, ParamState, bnb8_create_qmap, paged_prefetch, paged_zero_states, \
-    step as _step, zero_state
+from . import HParams, ParamState, bnb8_create_qmap, bnb8_workspace_size, paged_prefetch, \
+    paged_zero_states, step as _step, zero_state
 
 _HPARAM_KEYS = ("lr", "betas", "eps", "weight_decay", "optim_bits", "min_8bit_size", "max_unorm",
                 "skip_zeros", "alpha", "t_alpha", "t_beta3", "blocksize", "unorm_per_block")
@@ -86,7 +92,7 @@ class Optimizer8bit(torch.optim.Optimizer):
                  weight_decay=0.0, optim_bits=8, min_8bit_size=4096, max_unorm=0.0,
                  skip_zeros=False, alpha=0.0, t_alpha=0, t_beta3=0, blocksize=256,
                  unorm_per_block=False, is_paged=False, page_prefetch=True,
-                 manager: OptimManager | None = None):
+                 carry_pnorm=False, manager: OptimManager | None = None):
         if optim not in ("adam", "adamw", "momentum", "rmsprop", "adagrad", "lion", "ademamix"):
             raise ValueError(f"unknown optimizer {optim!r}")
         if optim_bits not in (8, 32):
@@ -100,8 +106,10 @@ class Optimizer8bit(torch.optim.Optimizer):
         self.optim = optim
         self.is_paged = bool(is_paged)
         self.page_prefetch = bool(page_prefetch)
+        self.carry_pnorm = bool(carry_pnorm)
         self.manager = manager or OptimManager.get_instance()
         self._maps = {}
+        self._carry_ws = {}  # batch -> workspace kept between steps (carry_pnorm)
 
     # ---- configuration ------------------------------------------------------
     def _config(self, group, p) -> dict:
@@ -200,8 +208,27 @@ class Optimizer8bit(torch.optim.Optimizer):
                 states.append(ParamState(p.data, p.grad, st["state1"], st.get("state2"),
                                          st.get("absmax1"), st.get("absmax2"), st["state_bits"]))
             q1, q2 = self._maps_for(params[0].device)
-            _step(states, hp, q1, q2, stream=stream)
+            ws = None
+            if (self.carry_pnorm and hp.max_unorm > 0 and not hp.unorm_per_block and
+                    hp.blocksize != 0 and not hp.skip_zeros):
+                hp.carry_pnorm = True
+                ws = self._carry_workspace((gi, dev, dtype, tuple(p.data_ptr() for p in params)),
+                                           states, hp)
+            _step(states, hp, q1, q2, workspace=ws, stream=stream)
         return loss
+
+    def _carry_workspace(self, key, states, hp):
+        need = bnb8_workspace_size(states, hp)
+        ws = self._carry_ws.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(need, dtype=torch.uint8, device=states[0].p.device)
+            self._carry_ws[key] = ws
+        return ws
+
+    def invalidate_carried_norms(self):
+        """Forget the carried ||p|| of every batch: call after changing
+        parameters outside step() when carry_pnorm is on."""
+        self._carry_ws.clear()
 
     # ---- checkpoints --------------------------------------------------------
     def load_state_dict(self, state_dict):
@@ -209,6 +236,7 @@ class Optimizer8bit(torch.optim.Optimizer):
         parameter to the parameter's dtype (uint8 codes included); here every
         state tensor keeps the dtype it was saved with, bit for bit."""
         saved = state_dict["state"]
+        self.invalidate_carried_norms()
         super().load_state_dict(state_dict)
         params = [(g, p) for g in self.param_groups for p in g["params"]]
         if self.is_paged:

@@ -132,7 +132,7 @@ typedef struct bnb8_tensor {
  *               max_unorm * ||p of the block|| is scaled down to it.  The
  *               norms are formed inside the step (no pre-pass, no workspace);
  *               the multiplier matches the binary64 definition to 1e-6.
- *               BNB8_TEST_STALL_WAIT: see enum bnb8_flags.
+ *               BNB8_CARRY_PNORM, BNB8_TEST_STALL_WAIT: see enum bnb8_flags.
  *               Other bits: BNB8_EINVAL.
  *   step        1-based number of this update (bias corrections, schedules). */
 typedef struct bnb8_hparams {
@@ -141,7 +141,7 @@ typedef struct bnb8_hparams {
   int32_t blocksize;
   int32_t skip_zeros;
   float lr, beta1, beta2, beta3, alpha, eps, weight_decay, gnorm_scale, max_unorm;
-  int32_t flags; /* 0, BNB8_UNORM_PER_BLOCK, BNB8_TEST_STALL_WAIT */
+  int32_t flags; /* 0 or BNB8_UNORM_PER_BLOCK, BNB8_CARRY_PNORM, BNB8_TEST_STALL_WAIT */
   int64_t step;
   int64_t t_alpha;
   int64_t t_beta3;
@@ -149,6 +149,23 @@ typedef struct bnb8_hparams {
 
 enum bnb8_flags {
   BNB8_UNORM_PER_BLOCK = 1, /* max_unorm per block instead of per tensor */
+  /* With max_unorm per tensor: the step also leaves, in the workspace, the
+   * per-block sums of the squares of the NEW parameters, stamped with the
+   * tensor list (its p pointers, sizes, state bits, block size, dtype and
+   * optimizer) and the step number.  The next call with step + 1, the same
+   * list and the same workspace finds the stamp and takes ||p|| for its
+   * max_unorm test from those sums: it reads no p for the norm, and none at
+   * all in the pre-pass when the update direction does not depend on p
+   * (decoupled weight decay, or weight_decay 0).  Any other call recomputes
+   * the norm; every pre-pass (bnb8_unorm included) clears the stamp, so a
+   * workspace shared between lists or calls only loses the shortcut.  The
+   * caller must not change p between the two calls, and a step that raised
+   * BNB8_STATUS_WAIT_TIMEOUT leaves no usable sums.  The sums are binary32
+   * per block, as the pre-pass forms them, but in the step's own summation
+   * order: the multiplier matches the binary64 definition to 1e-6 either
+   * way.  Tensor-wise steps (blocksize 0) and skip_zeros steps ignore the
+   * flag. */
+  BNB8_CARRY_PNORM = 2,
   /* Test hook of the bounded waits (not for training): in a plain step
    * (no skip_zeros, blocksize >= 256, max_unorm off or per tensor) one warp
    * of the step kernel withholds one of its own asynchronous copies, so its
@@ -223,8 +240,8 @@ int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const f
                               struct CUstream_st* stream);
 
 /* Bytes of workspace the step functions and bnb8_unorm need for this tensor
- * list: the per-tensor max_unorm pre-pass's partials (hp->max_unorm > 0
- * without BNB8_UNORM_PER_BLOCK) plus 16 bytes per tensor for tensor-wise
+ * list: the per-tensor max_unorm pre-pass's stamp, multipliers and partials
+ * (hp->max_unorm > 0 without BNB8_UNORM_PER_BLOCK) plus 16 bytes per tensor for tensor-wise
  * quantization (hp->blocksize 0); 0 when neither applies.  Returns 0 and
  * sets the error message on invalid arguments. */
 size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp);

@@ -107,6 +107,8 @@ def _configure(L):
                                      ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_double)]
     L.oracle_unorm_scale.restype = ctypes.c_float
+    L.oracle_param_sumsq.argtypes = [vp, ctypes.c_int, i64]
+    L.oracle_param_sumsq.restype = ctypes.c_double
     L.oracle_step.argtypes = [ctypes.POINTER(_HParams), vp, vp, vp, vp, vp, vp, i64,
                               ctypes.c_int, ctypes.c_int, i64, vp, vp]
     L.oracle_step.restype = ctypes.c_float
@@ -318,6 +320,14 @@ def unorm_scale(hp: HParams, t: TensorState, g: np.ndarray, dtype: str, blocksiz
                                  DTYPES[dtype], blocksize, _ptr(q1), _ptr(q2), ctypes.byref(U),
                                  ctypes.byref(P))
     return float(s), U.value, P.value
+
+
+def param_sumsq(p: np.ndarray, dtype: str) -> float:
+    """Sum of p^2 in binary64, in element order (p stored as ``dtype``): the
+    squared P of the max_unorm test, for the next step when p is the
+    parameter a step has just left."""
+    p = np.ascontiguousarray(p)
+    return float(lib().oracle_param_sumsq(_ptr(p), DTYPES[dtype], p.size))
 
 
 def step(hp: HParams, t: TensorState, g: np.ndarray, dtype: str, blocksize: int, q1=None,

@@ -46,6 +46,9 @@
  *  oracle_step (8-bit)       pinned: tracks the 32-bit torch optimizers within
  *                            the benchmark script's tolerances; skip_zeros and
  *                            max_unorm invariants; checkpoint round trip.
+ *  oracle_param_sumsq        pinned: Pythagorean closed forms in every
+ *                            dtype, exactly rounded sums (math.fsum), and the
+ *                            P of the next step's max_unorm test.
  */
 #include <math.h>
 #include <stdint.h>
@@ -500,6 +503,20 @@ float oracle_unorm_scale(const oracle_hparams* hp, const void* p, const void* g,
   double limit = (double)hp->max_unorm * pnorm;
   if (hp->max_unorm > 0.0f && unorm > limit) return (float)(limit / unorm);
   return 1.0f;
+}
+
+/* The squared parameter norm, sum of p[i]^2 in binary64 in element order.
+ * It is the P^2 of the max_unorm test above when p is the parameter as the
+ * call finds it, so for the parameter one step leaves it is the P^2 of the
+ * next step's test: the quantity a step that carries the norm forward forms
+ * while it writes p.  ([P2] max_unorm, as read above.) */
+double oracle_param_sumsq(const void* p, int dtype, int64_t n) {
+  double psum = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    const double v = (double)load_elem(p, dtype, i);
+    psum += v * v;
+  }
+  return psum;
 }
 
 /* READING (the alternative, per block): the same test with U and P taken

@@ -125,7 +125,7 @@ def _call2(L, tensors, hp, q1=FAKE, q2=FAKE, ws=None, wsb=0):
     (dict(dtype=7), b"dtype"),
     (dict(optim=bnb8.BNB8_LION), b"optimizer"),
     (dict(step=0), b"step"),
-    (dict(flags=2), b"flags"),
+    (dict(flags=4), b"flags"),
     (dict(max_unorm=-1.0), b"max_unorm"),
     (dict(max_unorm=float("nan")), b"max_unorm"),
     (dict(t_alpha=-1), b"t_alpha"),
@@ -172,7 +172,8 @@ def test_workspace_size_and_check(L):
     hp = _hp(max_unorm=1.0)
     need = L.bnb8_workspace_size(arr, 4, ctypes.byref(hp))
     blocks = 4 + 3 + 0 + 1
-    assert need == 256 + ((blocks * 8 + 255) // 256) * 256
+    # the carried norm's stamp, the multipliers, one float2 partial per block
+    assert need == 256 + 256 + ((blocks * 8 + 255) // 256) * 256
     assert _call2(L, ts, hp, ws=None, wsb=0) == bnb8.BNB8_EWORKSPACE
     assert _call2(L, ts, hp, ws=FAKE, wsb=need - 1) == bnb8.BNB8_EWORKSPACE
     assert _call2(L, ts, hp, ws=FAKE + 8, wsb=need) == bnb8.BNB8_EWORKSPACE

@@ -75,6 +75,12 @@ def test_algorithmic_bytes_model():
     wl = bench.WORKLOADS["momentum_embedding"]()
     n = 50257 * 1024
     assert wl.algorithmic_bytes(0.1) == int(2 * n + 0.1 * (6 * n + 8 * (n // 256)))
+    # a carried ||p|| spares the pre-pass its read of p (2 B/elem in bf16) only
+    # where the direction does not need p: decoupled decay, not Adam's coupled one
+    plain, carried = bench.WORKLOADS["gpt2xl_adamw"](), bench.WORKLOADS["gpt2xl_adamw_carried"]()
+    assert plain.algorithmic_bytes() - carried.algorithmic_bytes() == 2 * plain.elements
+    assert bench.WORKLOADS["gpt2xl"]().algorithmic_bytes() == \
+        bench.WORKLOADS["gpt2xl_carried"]().algorithmic_bytes()
 
 
 def test_clock_summary():
@@ -137,3 +143,62 @@ def test_codec_workloads_bytes_and_reference_arm(name, capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _cpu_params(wl, seed):
+    import torch
+    import bit_block_wise_gb300 as bnb8
+    import workloads
+    params, grads = [], []
+    for i, n in enumerate(wl.sizes):
+        nb = -(-n // wl.blocksize)
+        p = torch.from_numpy(workloads.normal(n, 0.02, seed + i))
+        s1 = torch.from_numpy(workloads.random_codes(n, seed + 10 + i))
+        s2 = torch.from_numpy(workloads.random_codes(n, seed + 20 + i))
+        a1 = torch.from_numpy(workloads.random_absmax(nb, 1e-3, seed + 30 + i))
+        a2 = torch.from_numpy(workloads.random_absmax(nb, 1e-6, seed + 40 + i))
+        params.append(bnb8.ParamState(p, None, s1, s2, a1, a2, 8))
+        grads.append(torch.from_numpy(workloads.normal(n, 1e-3, seed + 50 + i)))
+    return params, grads
+
+
+def _oracle_full_step(wl, params, grads, step):
+    # a stand-in for the GPU step that is right by construction: the oracle
+    # on the whole tensors
+    import torch
+    import oracle
+    q1, q2 = oracle.create_qmap(True), oracle.create_qmap(False)
+    for ps, g in zip(params, grads):
+        t = oracle.TensorState(ps.p.numpy().copy(), ps.s1.numpy().copy(), ps.s2.numpy().copy(),
+                               ps.absmax1.numpy().copy(), ps.absmax2.numpy().copy(), 8)
+        oracle.step(oracle.HParams(optim=wl.optim, step=step, **wl.hp), t, g.numpy(), "f32",
+                    wl.blocksize, q1, q2)
+        for dst, src in ((ps.p, t.p), (ps.s1, t.s1), (ps.s2, t.s2), (ps.absmax1, t.absmax1),
+                         (ps.absmax2, t.absmax2)):
+            dst.copy_(torch.from_numpy(src))
+
+
+@pytest.mark.parametrize("plant", [None, "code", "absmax", "p"])
+def test_sampled_parity_counts_what_differs(plant):
+    wl = bench.Workload("t", "t", "adam", "f32", [256 * 40 + 77], [8], 256,
+                        dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2),
+                        ("normal", 1e-3))
+    params, grads = _cpu_params(wl, 500)
+    ps = params[0]
+    n = ps.p.numel()
+
+    def gpu_step():
+        _oracle_full_step(wl, params, grads, 3)
+        if plant == "code":        # block 0 is always sampled; the last block too
+            ps.s1[5] = (int(ps.s1[5]) + 3) % 256
+        elif plant == "absmax":
+            ps.absmax2[-1] = ps.absmax2[-1] * 2
+        elif plant == "p":
+            ps.p[n - 1] = ps.p[n - 1] + 1.0
+
+    rep = bench.sampled_parity(wl, params, gpu_step, 3, grads)
+    assert rep["blocks"] >= 2 and rep["codes"] > 0 and rep["p_compared"] > 0
+    assert rep["code_mismatches"] == (1 if plant == "code" else 0)
+    assert rep["code_mismatch_max_index_delta"] == (3 if plant == "code" else 0)
+    assert rep["absmax_mismatches"] == (1 if plant == "absmax" else 0)
+    assert rep["p_mismatches"] == (1 if plant == "p" else 0)

@@ -136,3 +136,30 @@ def test_override_config_per_parameter(bnb8):
     assert opt.state[w]["state_bits"] == 32 and opt.state[w]["state1"].dtype == torch.float32
     assert torch.equal(m[2].weight, before)          # lr 0 for that weight
     assert not torch.equal(m[0].bias, _model(torch.float32, 3)[0].bias)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_carry_pnorm_matches_the_plain_pre_pass(bnb8, dtype):
+    # AdamW (decoupled decay): the states never see p, so carrying ||p|| may
+    # change p only through the multiplier's last bits (a different summation
+    # order of the same binary32 partials)
+    from bit_block_wise_gb300 import optim as O
+    plain = _model(dtype, 5)
+    carried = copy.deepcopy(plain)
+    kw = dict(max_unorm=0.02, weight_decay=1e-2, manager=O.OptimManager())
+    opt_p = O.AdamW8bit(plain.parameters(), **kw)
+    opt_c = O.AdamW8bit(carried.parameters(), carry_pnorm=True, **kw)
+    _train(plain, opt_p, 5, dtype)
+    _train(carried, opt_c, 5, dtype)
+    torch.cuda.synchronize()
+    assert len(opt_c._carry_ws) >= 1 and len(opt_p._carry_ws) == 0
+    for ws in opt_c._carry_ws.values():
+        assert int(ws[:8].view(torch.int64).item()) != 0     # a step left its stamp
+    tol = 1e-6 if dtype == torch.float32 else 2.0 ** -7
+    for a, b in zip(plain.parameters(), carried.parameters()):
+        assert torch.allclose(a.float(), b.float(), rtol=tol, atol=0.0)
+        for key in ("state1", "state2", "absmax1", "absmax2"):
+            if key in opt_p.state[a]:
+                assert torch.equal(opt_p.state[a][key], opt_c.state[b][key]), key
+    opt_c.load_state_dict(opt_c.state_dict())
+    assert len(opt_c._carry_ws) == 0

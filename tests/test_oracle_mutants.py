@@ -107,6 +107,17 @@ MUTANTS = [
     ("per-block parameter norm after the step", "    psum += (double)pv * (double)pv;\n  }\n  double unorm = sc->unorm_c",
      "    psum += (double)r.p * (double)r.p;\n  }\n  double unorm = sc->unorm_c",
      [(pins.test_max_unorm_per_block_invariants, ("adam", 8))]),
+    ("parameter norm without squares", "    psum += v * v;\n  }\n  return psum;",
+     "    psum += fabs(v);\n  }\n  return psum;",
+     [(pins.test_param_sumsq_closed_forms, ("f32",))]),
+    ("parameter norm drops the last element",
+     "for (int64_t i = 0; i < n; ++i) {\n    const double v = (double)load_elem(p, dtype, i);",
+     "for (int64_t i = 0; i + 1 < n; ++i) {\n    const double v = (double)load_elem(p, dtype, i);",
+     [(pins.test_param_sumsq_closed_forms, ("bf16",))]),
+    ("parameter norm squares in binary32",
+     "const double v = (double)load_elem(p, dtype, i);\n    psum += v * v;",
+     "const float v = load_elem(p, dtype, i);\n    psum += (double)(v * v);",
+     [(pins.test_param_sumsq_matches_an_exactly_rounded_sum, ())]),
     ("bf16 rounds half up", "u += 0x7fffu + kept_lsb;", "u += 0x8000u;",
      [(pins.test_bf16_rounding_matches_torch, ())]),
     ("f16 subnormals truncated", "nearbyintf(fa * 16777216.0f)", "floorf(fa * 16777216.0f)",

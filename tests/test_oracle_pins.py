@@ -689,6 +689,78 @@ def test_max_unorm_norms_match_numpy():
     assert abs(scale - expect) <= 1e-6 * expect
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_param_sumsq_closed_forms(dtype):
+    # Pythagorean quadruples and sign: every value is exact in all three dtypes
+    p = oracle.to_storage(np.array([2.0, -3.0, 6.0, 1.0, -2.0, 2.0], np.float32), dtype)
+    assert oracle.param_sumsq(p, dtype) == 4 + 9 + 36 + 1 + 4 + 4
+    ones = oracle.to_storage(np.full(1000, -0.5, np.float32), dtype)
+    assert oracle.param_sumsq(ones, dtype) == 250.0
+    assert oracle.param_sumsq(oracle.to_storage(np.zeros(0, np.float32), dtype), dtype) == 0.0
+    # the squares are taken of the stored values (rounded to the dtype), not of
+    # the binary32 inputs
+    x = np.array([1.0 + 2.0 ** -12], np.float32)
+    stored = float(oracle.to_f32(oracle.to_storage(x, dtype), dtype)[0])
+    assert oracle.param_sumsq(oracle.to_storage(x, dtype), dtype) == stored * stored
+    if dtype != "f32":
+        assert stored == 1.0
+
+
+def test_param_sumsq_matches_an_exactly_rounded_sum():
+    p = workloads.normal(100000, 0.02, 140)
+    exact = math.fsum(float(v) * float(v) for v in p.astype(np.float64))
+    got = oracle.param_sumsq(p, "f32")
+    # n * 2^-53 relative bound of a recursive binary64 sum of positive terms
+    assert abs(got - exact) <= 100000 * 2.0 ** -53 * exact
+
+
+@pytest.mark.parametrize("optim,wd", [("adam", 0.0), ("adam", 0.1), ("adamw", 0.1),
+                                      ("momentum", 0.0), ("lion", 0.1), ("ademamix", 0.1)])
+def test_next_step_norm_is_the_norm_this_step_leaves(optim, wd):
+    # the norm a step can carry forward: after step k, the P of step k + 1's
+    # max_unorm test is the norm of the p step k wrote (decay included)
+    q1, q2 = MAPS[optim]
+    n, B = 1500, 256
+    s1, s2, a1, a2 = _random_8bit_state(optim, n, B, 141, q1, q2)
+    t = oracle.TensorState(workloads.normal(n, 0.02, 142), s1, s2, a1, a2, 8)
+    hpkw = dict(optim=optim, lr=1e-3, alpha=2.0, weight_decay=wd, max_unorm=0.05)
+    for k in (1, 2, 3):
+        oracle.step(oracle.HParams(step=k, **hpkw), t, workloads.normal(n, 1e-2, 143 + k),
+                    "f32", B, q1, q2)
+        _, _, pnorm = oracle.unorm_scale(oracle.HParams(step=k + 1, **hpkw), t,
+                                         workloads.normal(n, 1e-2, 150 + k), "f32", B, q1, q2)
+        want = np.linalg.norm(t.p.astype(np.float64))
+        assert abs(pnorm - want) <= 1e-12 * want
+        assert pnorm == math.sqrt(oracle.param_sumsq(t.p, "f32"))
+
+
+@pytest.mark.parametrize("optim,wd,depends", [("adam", 0.0, False), ("adam", 0.1, True),
+                                              ("adamw", 0.1, False), ("lion", 0.1, False),
+                                              ("momentum", 0.1, True),
+                                              ("ademamix", 0.1, False)])
+def test_update_norm_depends_on_p_only_through_coupled_decay(optim, wd, depends):
+    # the reading that lets a pre-pass with a carried ||p|| skip reading p: the
+    # update direction's norm U involves p only through weight decay added to
+    # the gradient (coupled); decoupled decay is applied to p after the
+    # direction, outside U
+    q1, q2 = MAPS[optim]
+    n, B = 1200, 256
+    s1, s2, a1, a2 = _random_8bit_state(optim, n, B, 160, q1, q2)
+    g = workloads.normal(n, 1e-2, 161)
+    hp = oracle.HParams(optim=optim, lr=1e-3, alpha=2.0, weight_decay=wd, max_unorm=0.05,
+                        step=3)
+    us = []
+    for seed in (162, 163):
+        t = oracle.TensorState(workloads.normal(n, 0.5, seed), s1.copy(),
+                               None if s2 is None else s2.copy(), a1.copy(),
+                               None if a2 is None else a2.copy(), 8)
+        us.append(oracle.unorm_scale(hp, t, g, "f32", B, q1, q2)[1])
+    if depends:
+        assert abs(us[0] - us[1]) > 1e-6 * us[0]
+    else:
+        assert us[0] == us[1]
+
+
 @pytest.mark.parametrize("optim,bits", [("adam", 8), ("momentum", 8), ("lion", 8),
                                          ("adam", 32)])
 def test_max_unorm_per_block_invariants(optim, bits):

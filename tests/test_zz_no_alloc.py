@@ -2,8 +2,9 @@
 device memory (every byte handed out by a host framework's pool, or a hot loop
 where cudaMalloc / cudaFree would stall the device).  It keeps its partial
 norms in a fixed scratch array inside the library instead of a caller
-workspace.  Its results must equal bnb8_unorm's (which uses a workspace) call
-after call, although the array keeps whatever the previous call left in it.
+workspace.  It must give bnb8_unorm's (workspace) results bit for bit, and the
+oracle's multipliers to 1e-6, call after call, although the array keeps
+whatever the previous call left in it.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test."""
@@ -29,40 +30,58 @@ def bnb8():
     return m
 
 
-def _tensor_list(bnb8, optim, sizes, bits, seed):
-    import torch
+def _tensor_list(bnb8, optim, sizes, bits, seed, p_scale=1.0):
     q1, q2 = map_pair(optim, S, U)
-    params = []
+    params, refs = [], []
     for i, (n, b) in enumerate(zip(sizes, bits)):
         st = random_state(optim, n, b, 256, seed + 10 * i, q1, q2)
-        params.append(bnb8.ParamState(to_dev(workloads.normal(n, 0.02, seed + 10 * i + 5)),
-                                      to_dev(workloads.normal(n, 1e-2, seed + 10 * i + 6)),
-                                      *[to_dev(a) for a in st], b))
-    return params, q1, q2
+        p = (workloads.normal(n, 0.02, seed + 10 * i + 5) * np.float32(p_scale)).astype(np.float32)
+        g = workloads.normal(n, 1e-2, seed + 10 * i + 6)
+        refs.append((oracle.TensorState(p.copy(), *st, b), g))
+        params.append(bnb8.ParamState(to_dev(p), to_dev(g), *[to_dev(a) for a in st], b))
+    return params, refs, q1, q2
+
+
+def _out(n):
+    import torch
+    return torch.empty(n, dtype=torch.float32, device="cuda")
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
-def test_static_scratch_matches_workspace_version_twice(bnb8, optim):
+def test_static_scratch_matches_workspace_version_and_oracle_twice(bnb8, optim):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    hp = bnb8.HParams(optim=optim, max_unorm=0.02, step=4, lr=1e-3, beta1=0.9, beta2=0.999,
-                      alpha=2.0)
-    # two calls in a row; the second list is smaller than the first, so stale
-    # partials from the first call sit in the array beyond what it writes
-    cases = [([70000, 700, 256 * 300 + 3], [8, 32, 8], 100),
-             ([5000, 1234], [8, 8], 200)]
-    for sizes, bits, seed in cases:
-        params, q1, q2 = _tensor_list(bnb8, optim, sizes, bits, seed)
-        qd1 = to_dev(q1)
-        qd2 = None if q2 is None else to_dev(q2)
-        want = bnb8.bnb8_unorm(params, hp, qd1, qd2)
-        got = bnb8.bnb8_unorm_static(params, hp, qd1, qd2)
-        torch.cuda.synchronize()
-        w, g = to_host(want), to_host(got)
-        assert np.all(w < 1.0)                       # the clip is active in these cases
-        np.testing.assert_allclose(g, w, rtol=1e-6, atol=0)
+    hp = dict(optim=optim, max_unorm=0.02, step=4, lr=1e-3, beta1=0.9, beta2=0.999, alpha=2.0)
+    bhp, ohp = bnb8.HParams(**hp), oracle.HParams(**hp)
+    # First call: parameters of 1e30 make every partial norm of this call
+    # non-finite (p^2 overflows), so that the second, smaller list would
+    # change its multipliers if it read any partial it did not write itself.
+    params, _, q1, q2 = _tensor_list(bnb8, optim, [70000, 700, 256 * 300 + 3], [8, 32, 8], 100,
+                                     p_scale=5e31)
+    qd1 = to_dev(q1)
+    qd2 = None if q2 is None else to_dev(q2)
+    first_ws = bnb8.bnb8_unorm(params, bhp, qd1, qd2)
+    first = bnb8.bnb8_unorm_static(params, bhp, qd1, qd2, out_scale=_out(len(params)))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(first), to_host(first_ws))
+    # Second call: an ordinary list with fewer blocks than the first wrote.
+    params, refs, q1, q2 = _tensor_list(bnb8, optim, [5000, 1234], [8, 8], 200)
+    want = bnb8.bnb8_unorm(params, bhp, qd1, qd2)
+    got = bnb8.bnb8_unorm_static(params, bhp, qd1, qd2, out_scale=_out(len(params)))
+    torch.cuda.synchronize()
+    w, gt = to_host(want), to_host(got)
+    np.testing.assert_array_equal(gt, w)             # same kernels and summation order
+    assert np.all(w < 1.0)                           # the clip is active in this case
+    for i, (ref, g) in enumerate(refs):
+        scale, _, _ = oracle.unorm_scale(ohp, ref, g, "f32", 256, q1, q2)
+        assert abs(float(gt[i]) - scale) <= 1e-6 * scale, (i, float(gt[i]), scale)
+
+
+def test_static_scratch_needs_an_output_buffer(bnb8):
+    with pytest.raises(ValueError):
+        bnb8.bnb8_unorm_static([], bnb8.HParams(max_unorm=1.0), None)
 
 
 def test_static_scratch_rejects_lists_beyond_its_size(bnb8):
