@@ -365,7 +365,9 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
   a.qmap2 = qmap2;
   int64_t fb = 0;
   a.whole = 1;
-  const int64_t unit = (int64_t(1) << log2B) > 256 ? (int64_t(1) << log2B) : 256;
+  a.ring_units = 0;
+  const int log2U = log2B > 9 ? log2B : 9;  // a ring unit: max(512, B) elements
+  const int64_t unit = int64_t(1) << log2U;
   for (size_t k = 0; k < c.idx.size(); ++k) {
     const bnb8_tensor& t = ts[c.idx[k]];
     DevTensor& d = a.t[k];
@@ -380,6 +382,8 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
     d.index = c.idx[k];
     d.vec_ok = plan.vec[c.idx[k]];
     d.nblocks = static_cast<int32_t>((t.n + (int64_t(1) << log2B) - 1) >> log2B);
+    d.units = static_cast<int32_t>((t.n + unit - 1) >> log2U);
+    a.ring_units += d.units;
     if (d.vec_ok != 3 || t.n % unit != 0) a.whole = 0;
     fb += d.nblocks;
   }

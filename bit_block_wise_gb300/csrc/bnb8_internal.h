@@ -57,10 +57,10 @@ struct DevTensor {
   int64_t first_block;  // index of the tensor's first block in the launch
   int32_t index;        // position in the caller's tensor list (clip / out_scale slot)
   // bit 0: every stream of this tensor is aligned for vector access; bit 1:
-  // also for 16-byte bulk copies of whole 256-element chunks
+  // also for 16-byte bulk copies of whole chunks (multiples of 256 elements)
   int32_t vec_ok;
   int32_t nblocks;      // ceil(n / B)
-  int32_t reserved;
+  int32_t units;        // the ring step's work units: ceil(n / max(512, B))
 };
 
 // Per-step scalars (host: binary64, rounded once) and the tensor table.
@@ -89,8 +89,9 @@ struct StepArgs {
   int32_t nsm;             // SMs of the device (persistent grids sized in the launcher)
   int32_t stall_test;      // test hook: one warp withholds a copy so that its wait runs out
   // 1 if every tensor of the launch has vec_ok == 3 and n a multiple of
-  // max(256, B): all its 256-element chunks are whole and bulk-copyable
+  // max(512, B): all its 512-element chunks are whole and bulk-copyable
   int32_t whole;
+  int64_t ring_units;      // sum of DevTensor::units
   uint64_t wait_ns;        // bound of every wait for an async copy
   uint32_t* status;        // the library's device status word (kStatus* bits are or-ed in)
   // The carried parameter norm (BNB8_CARRY_PNORM): a MODE_STEP launch with
