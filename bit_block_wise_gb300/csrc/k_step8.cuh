@@ -564,8 +564,7 @@ cudaError_t launch_step8_skip(const StepArgs& a, int grid, cudaStream_t s) {
 template <int OPT, int DT, int MODE>
 cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
   // the plain step over blocks of 256 elements or more: the async-copy ring
-  // (AdEMAMix's three code streams do not fit its register budget yet)
-  if constexpr (OPT != ADEMAMIX && MODE == MODE_STEP) {
+  if constexpr (MODE == MODE_STEP) {
     if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0) return launch_step8_ring<OPT, DT>(a, s);
   }
   return a.skip_zeros ? launch_step8_skip<OPT, DT, MODE, true>(a, grid, s)
