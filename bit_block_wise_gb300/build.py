@@ -17,7 +17,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbnb8.so")
-SOURCES = ["bnb8_api.cu", "k_quant.cu", "k_step_adam.cu", "k_step_1state.cu", "k_step_ademamix.cu"]
+# (source, object, extra flags): the step kernels compile once per optimizer
+OPTIMIZERS = ["adam", "adamw", "momentum", "rmsprop", "adagrad", "lion", "ademamix"]
+UNITS = [("bnb8_api.cu", "bnb8_api.o", []), ("k_quant.cu", "k_quant.o", [])] + [
+    ("k_step_opt.cu", f"k_step_{name}.o", [f"-DBNB8_OPT={i}"]) for i, name in enumerate(OPTIMIZERS)]
+SOURCES = sorted({src for src, _, _ in UNITS})
 HEADERS = ["bnb8_internal.h", "bnb8_device.cuh", "k_step8.cuh", "k_step8_ring.cuh", "k_step32.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -46,14 +50,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(OBJ, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "bnb8.h")]
     jobs = []
-    for src in SOURCES:
+    for src, obj, extra in UNITS:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src.replace(".cu", ".o"))
+        o = os.path.join(OBJ, obj)
         if force or ptxas_info or _stale(o, [s] + hdrs):
-            cmd = [nvcc(), *NVCC_FLAGS, "-c", s, "-o", o]
+            cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", s, "-o", o]
             if ptxas_info:
                 cmd += ["-Xptxas", "-v"]
-            jobs.append((src, cmd))
+            jobs.append((obj, cmd))
     outputs = {}
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
@@ -64,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 outputs[futs[f]] = r.stderr + r.stdout
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed for {futs[f]}:\n{r.stderr}{r.stdout}")
-    objs = [os.path.join(OBJ, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(OBJ, obj) for _, obj, _ in UNITS]
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]

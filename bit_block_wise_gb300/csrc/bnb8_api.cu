@@ -392,9 +392,29 @@ StepArgs make_args(const Plan::Chunk& c, const bnb8_tensor* ts, const Plan& plan
 
 cudaError_t launch_family(int bits, int optim, int dtype, int mode, const StepArgs& a, int grid,
                           cudaStream_t s) {
-  if (optim == BNB8_ADAM || optim == BNB8_ADAMW) return launch_step_adam(bits, optim, dtype, mode, a, grid, s);
-  if (optim == BNB8_ADEMAMIX) return launch_step_ademamix(bits, optim, dtype, mode, a, grid, s);
-  return launch_step_1state(bits, optim, dtype, mode, a, grid, s);
+  switch (optim) {
+    case BNB8_ADAM: return launch_step_opt<ADAM>(bits, dtype, mode, a, grid, s);
+    case BNB8_ADAMW: return launch_step_opt<ADAMW>(bits, dtype, mode, a, grid, s);
+    case BNB8_MOMENTUM: return launch_step_opt<MOMENTUM>(bits, dtype, mode, a, grid, s);
+    case BNB8_RMSPROP: return launch_step_opt<RMSPROP>(bits, dtype, mode, a, grid, s);
+    case BNB8_ADAGRAD: return launch_step_opt<ADAGRAD>(bits, dtype, mode, a, grid, s);
+    case BNB8_LION: return launch_step_opt<LION>(bits, dtype, mode, a, grid, s);
+    case BNB8_ADEMAMIX: return launch_step_opt<ADEMAMIX>(bits, dtype, mode, a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t tw_store_family(int optim, const StepArgs& a, cudaStream_t s) {
+  switch (optim) {
+    case BNB8_ADAM: return tw_store_opt<ADAM>(a, s);
+    case BNB8_ADAMW: return tw_store_opt<ADAMW>(a, s);
+    case BNB8_MOMENTUM: return tw_store_opt<MOMENTUM>(a, s);
+    case BNB8_RMSPROP: return tw_store_opt<RMSPROP>(a, s);
+    case BNB8_ADAGRAD: return tw_store_opt<ADAGRAD>(a, s);
+    case BNB8_LION: return tw_store_opt<LION>(a, s);
+    case BNB8_ADEMAMIX: return tw_store_opt<ADEMAMIX>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int log2B) {
@@ -403,9 +423,15 @@ int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int
   std::atomic<int>& slot = cache[bits == 8 ? 0 : 1][optim][dtype][mode];
   int c = slot.load(std::memory_order_relaxed);
   if (c == 0) {
-    if (optim == BNB8_ADAM || optim == BNB8_ADAMW) c = ctas_step_adam(bits, optim, dtype, mode);
-    else if (optim == BNB8_ADEMAMIX) c = ctas_step_ademamix(bits, optim, dtype, mode);
-    else c = ctas_step_1state(bits, optim, dtype, mode);
+    switch (optim) {
+      case BNB8_ADAM: c = ctas_step_opt<ADAM>(bits, dtype, mode); break;
+      case BNB8_ADAMW: c = ctas_step_opt<ADAMW>(bits, dtype, mode); break;
+      case BNB8_MOMENTUM: c = ctas_step_opt<MOMENTUM>(bits, dtype, mode); break;
+      case BNB8_RMSPROP: c = ctas_step_opt<RMSPROP>(bits, dtype, mode); break;
+      case BNB8_ADAGRAD: c = ctas_step_opt<ADAGRAD>(bits, dtype, mode); break;
+      case BNB8_LION: c = ctas_step_opt<LION>(bits, dtype, mode); break;
+      default: c = ctas_step_opt<ADEMAMIX>(bits, dtype, mode); break;
+    }
     slot.store(c, std::memory_order_relaxed);
   }
   const int groups_per_cta = kThreads / ((1 << log2B) >> 3);
@@ -540,7 +566,7 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
       if (c.bits != 8) continue;
       StepArgs a = make_args(c, ts, plan, *hp, sc, log2B, qmap1, qmap2);
       a.tw_acc = tw_acc;
-      const cudaError_t e = launch_tw_store(hp->optim, a, stream);
+      const cudaError_t e = tw_store_family(hp->optim, a, stream);
       if (e != cudaSuccess) return cuda_fail(e, "tensor-wise store launch");
     }
   }

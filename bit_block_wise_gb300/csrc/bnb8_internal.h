@@ -147,24 +147,37 @@ struct FinalizeArgs {
 
 // Kernel launchers (defined in the kernel translation units).  Each returns
 // the cudaError_t of its launch.  bits = 8 (block-wise codes) or 32.
-cudaError_t launch_step_adam(int bits, int optim, int dtype, int mode, const StepArgs& a, int grid,
-                             cudaStream_t s);
-cudaError_t launch_step_1state(int bits, int optim, int dtype, int mode, const StepArgs& a,
-                               int grid, cudaStream_t s);
-cudaError_t launch_step_ademamix(int bits, int optim, int dtype, int mode, const StepArgs& a,
-                                 int grid, cudaStream_t s);
+// One optimizer's kernels (k_step_opt.cu, compiled once per optimizer): the
+// step in each mode, its resident CTAs per SM, and tensor-wise
+// quantization's last step (the new absmax of every tensor of a launch from
+// tw_acc into its absmax arrays, tensors with an update only).
+template <int OPT>
+cudaError_t launch_step_opt(int bits, int dtype, int mode, const StepArgs& a, int grid, cudaStream_t s);
+template <int OPT>
+int ctas_step_opt(int bits, int dtype, int mode);
+template <int OPT>
+cudaError_t tw_store_opt(const StepArgs& a, cudaStream_t s);
+#define BNB8_DECLARE_OPT(OPTV)                                                                \
+  template <>                                                                                 \
+  cudaError_t launch_step_opt<OPTV>(int, int, int, const StepArgs&, int, cudaStream_t);      \
+  template <>                                                                                 \
+  int ctas_step_opt<OPTV>(int, int, int);                                                     \
+  template <>                                                                                 \
+  cudaError_t tw_store_opt<OPTV>(const StepArgs&, cudaStream_t);
+BNB8_DECLARE_OPT(ADAM)
+BNB8_DECLARE_OPT(ADAMW)
+BNB8_DECLARE_OPT(MOMENTUM)
+BNB8_DECLARE_OPT(RMSPROP)
+BNB8_DECLARE_OPT(ADAGRAD)
+BNB8_DECLARE_OPT(LION)
+BNB8_DECLARE_OPT(ADEMAMIX)
+#undef BNB8_DECLARE_OPT
 cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);  // both levels
 cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s);
-// Tensor-wise quantization's last step: the new absmax of every tensor of a
-// launch from tw_acc into its absmax arrays (tensors with an update only).
-cudaError_t launch_tw_store(int optim, const StepArgs& a, cudaStream_t s);
 
 // Resident CTAs per SM of a step kernel (sizes the persistent grids).
-int ctas_step_adam(int bits, int optim, int dtype, int mode);
-int ctas_step_1state(int bits, int optim, int dtype, int mode);
-int ctas_step_ademamix(int bits, int optim, int dtype, int mode);
 int quantize_ctas_per_sm(int dtype);
 
 }  // namespace bnb8

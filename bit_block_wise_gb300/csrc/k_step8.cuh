@@ -563,9 +563,11 @@ cudaError_t launch_step8_skip(const StepArgs& a, int grid, cudaStream_t s) {
 
 template <int OPT, int DT, int MODE>
 cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
-  // the plain step over blocks of 256 elements or more: the async-copy ring
-  if constexpr (MODE == MODE_STEP) {
-    if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0) return launch_step8_ring<OPT, DT>(a, s);
+  // the plain step and its max_unorm pre-pass over blocks of 256 elements or
+  // more: the async-copy ring
+  if constexpr (MODE == MODE_STEP || MODE == MODE_NORM) {
+    if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0)
+      return launch_step8_ring<OPT, DT, MODE == MODE_NORM>(a, s);
   }
   return a.skip_zeros ? launch_step8_skip<OPT, DT, MODE, true>(a, grid, s)
                       : launch_step8_skip<OPT, DT, MODE, false>(a, grid, s);

@@ -382,11 +382,35 @@ __device__ __forceinline__ float ring_group_sum(float v, int G, int warp, int la
   return v;
 }
 
+// Sums of (x, y) over the G warps of a group (G > 1), in a fixed order.
+__device__ __forceinline__ float2 ring_group_sum2(float2 v, int G, int warp, int lane, uint32_t* red,
+                                                  int parity) {
+  float* slot = reinterpret_cast<float*>(red + parity * 32 * 4);
+  if (lane == 0) {
+    slot[warp * 4] = v.x;
+    slot[warp * 4 + 1] = v.y;
+  }
+  const int grp = warp / G;
+  named_barrier(1 + grp, G * 32);
+  const int w0 = grp * G;
+  float2 acc = make_float2(slot[w0 * 4], slot[w0 * 4 + 1]);
+  for (int w = 1; w < G; ++w) {
+    acc.x += slot[(w0 + w) * 4];
+    acc.y += slot[(w0 + w) * 4 + 1];
+  }
+  return acc;
+}
+
 // WHOLE: every tensor of the launch is aligned for bulk copies and a
 // multiple of max(512, B) elements, so every chunk is whole and streams
 // through the ring; the element-wise paths for ragged or misaligned chunks are
 // compiled out.  SEQ: blocksize 256, two passes per chunk (RingShape).
-template <int OPT, int DT, bool WHOLE, bool SEQ>
+// NORM: the per-tensor max_unorm pre-pass instead of the step: the same
+// update directions u, summed per block as (sum u^2, sum p^2) into
+// StepArgs::partials; nothing else is written.  With a carried norm
+// (BNB8_CARRY_PNORM) the p^2 sums are already there, and p is not even read
+// when the direction does not need it.
+template <int OPT, int DT, bool WHOLE, bool SEQ, bool NORM>
 __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
     k_step8_ring(const __grid_constant__ StepArgs a) {
   using L = RingSmem<OPT, DT, SEQ>;
@@ -421,6 +445,9 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
   const int32_t NG = static_cast<int32_t>(gridDim.x) * gpc;
   const int32_t b0 = static_cast<int32_t>(blockIdx.x) * gpc + warp / G;
   const int32_t TB = static_cast<int32_t>(a.ring_units);
+  // the pre-pass with a carried parameter norm
+  const bool carried = NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
+  const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));
 
   // ---- the ring: barriers, then the first chunks' copies ----
   if (lane < kStages) mbar_init(bars + lane, 2);   // the bulk copies' arrival and the absmax copies'
@@ -432,8 +459,9 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
   auto issue = [&](const ChunkRef& c, int s) {
     const DevTensor& d = a.t[c.t];
     unsigned char* st = ring + s * L::kStage;
-    mbar_expect_tx(bars + s, L::kSA);
-    bulk_g2s(st + L::kSP, static_cast<const unsigned char*>(d.p) + c.e0 * ES, kChunk * ES, bars + s);
+    mbar_expect_tx(bars + s, read_p ? L::kSA : L::kSA - kChunk * ES);
+    if (read_p)
+      bulk_g2s(st + L::kSP, static_cast<const unsigned char*>(d.p) + c.e0 * ES, kChunk * ES, bars + s);
     bulk_g2s(st + L::kSG, static_cast<const unsigned char*>(d.g) + c.e0 * ES, kChunk * ES, bars + s);
 #pragma unroll
     for (int k = 0; k < NS; ++k)
@@ -553,7 +581,12 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       float p[NE], g[NE];
       uint32_t cw[NS][NQ];
       if (staged) {
-        stage_load<DT, NQ>(st + L::kSP, lane, q0, p);
+        if (read_p) {
+          stage_load<DT, NQ>(st + L::kSP, lane, q0, p);
+        } else {
+#pragma unroll
+          for (int e = 0; e < NE; ++e) p[e] = 0.0f;
+        }
         stage_load<DT, NQ>(st + L::kSG, lane, q0, g);
 #pragma unroll
         for (int k = 0; k < NS; ++k) stage_codes<DT, NQ>(st + L::kSC + k * kChunk, lane, q0, cw[k]);
@@ -577,7 +610,12 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             am[1][k] = second ? absmax_stream<OPT>(d, k)[lb0 + 1] : am[0][k];
           }
         }
-        global_load<DT, NQ>(d.p, c.e0, c.v, lane, q0, p);
+        if (read_p) {
+          global_load<DT, NQ>(d.p, c.e0, c.v, lane, q0, p);
+        } else {
+#pragma unroll
+          for (int e = 0; e < NE; ++e) p[e] = 0.0f;
+        }
         global_load<DT, NQ>(d.g, c.e0, c.v, lane, q0, g);
 #pragma unroll
         for (int k = 0; k < NS; ++k)
@@ -589,11 +627,19 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       // ---- block half in mx ----
       float sv[NS][NE];
       uint32_t mx[2][NS];
-      float psq[2] = {0.0f, 0.0f};   // sum of the new p^2 per block half (the carried norm)
+      float psq[2] = {0.0f, 0.0f};   // sum of p^2 per block half (carried norm; NORM: the old p)
+      float usq[2] = {0.0f, 0.0f};   // NORM: sum of u^2 per block half
 #pragma unroll
       for (int k = 0; k < NS; ++k) mx[0][k] = mx[1][k] = 0u;
       // the block half of element e of this pass
       auto half_of = [](int e) { return SEQ ? 0 : (e >> 3); };
+      // element e of this pass is present (partial chunks)
+      const bool full = WHOLE || c.v == kChunk;
+      auto present = [&](int e) { return full || quad_offset<DT>(lane, q0 + (e >> 2)) + (e & 3) < c.v; };
+      // NORM: one element's direction into its block half's sum
+      auto add_u = [&](int e, float u) {
+        if (present(e)) usq[half_of(e)] = usq[half_of(e)] + u * u;
+      };
       if (have_p) {
         // optimizers whose direction is n / (sqrt(v) + eps)
         constexpr bool kRatio = OPT == ADAM || OPT == ADAMW || OPT == RMSPROP || OPT == ADAGRAD ||
@@ -648,8 +694,13 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
           } else if (OPT == MOMENTUM) {
             const float2 m = fma2(f2(a.b1), stt[0], gg);
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
-            pair_apply<OPT>(a, -eff, pp, m);
-            p[e] = pp.x; p[e + 1] = pp.y;
+            if (NORM) {
+              add_u(e, m.x);
+              add_u(e + 1, m.y);
+            } else {
+              pair_apply<OPT>(a, -eff, pp, m);
+              p[e] = pp.x; p[e + 1] = pp.y;
+            }
           } else {  // LION
             const float2 cc = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
             float2 u;
@@ -657,8 +708,13 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
             const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
-            pair_apply<OPT>(a, -eff, pp, u);
-            p[e] = pp.x; p[e + 1] = pp.y;
+            if (NORM) {
+              add_u(e, u.x);
+              add_u(e + 1, u.y);
+            } else {
+              pair_apply<OPT>(a, -eff, pp, u);
+              p[e] = pp.x; p[e + 1] = pp.y;
+            }
           }
         }
         // absent elements of a partial chunk keep state 0 (they do not count in the absmax)
@@ -699,22 +755,41 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              float2 pp = make_float2(p[e], p[e + 1]);
-              pair_apply<OPT>(a, -eff, pp, u);
-              p[e] = pp.x; p[e + 1] = pp.y;
+              if (NORM) {
+                add_u(e, u.x);
+                add_u(e + 1, u.y);
+              } else {
+                float2 pp = make_float2(p[e], p[e + 1]);
+                pair_apply<OPT>(a, -eff, pp, u);
+                p[e] = pp.x; p[e + 1] = pp.y;
+              }
             }
           } else {
 #pragma unroll
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              float2 pp = make_float2(p[e], p[e + 1]);
-              pair_apply<OPT>(a, -eff, pp, u);
-              p[e] = pp.x; p[e + 1] = pp.y;
+              if (NORM) {
+                add_u(e, u.x);
+                add_u(e + 1, u.y);
+              } else {
+                float2 pp = make_float2(p[e], p[e + 1]);
+                pair_apply<OPT>(a, -eff, pp, u);
+                p[e] = pp.x; p[e + 1] = pp.y;
+              }
             }
           }
         }
-        ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
-        if (a.carry_out) {
+        if (NORM) {
+          // the parameter norm of the step's input (unless carried)
+          if (!carried) {
+#pragma unroll
+            for (int e = 0; e < NE; ++e)
+              if (present(e)) psq[half_of(e)] = psq[half_of(e)] + p[e] * p[e];
+          }
+        } else {
+          ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
+        }
+        if (!NORM && a.carry_out) {
           // the squares of p as stored (rounded to the dtype); the registers
           // of a partial chunk's absent elements hold no parameter
 #pragma unroll
@@ -729,6 +804,47 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
         for (int k = 0; k < NS; ++k)
 #pragma unroll
           for (int e = 0; e < NE; ++e) sv[k][e] = 0.0f;
+      }
+
+      if constexpr (NORM) {
+        // ---- the blocks' (sum u^2, sum p^2) ----
+        if (SEQ || two) {
+          float2 r0 = make_float2(usq[0], psq[0]), r1 = make_float2(usq[1], psq[1]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            r0.x += __shfl_xor_sync(0xffffffffu, r0.x, o);
+            r0.y += __shfl_xor_sync(0xffffffffu, r0.y, o);
+            if (!SEQ) {
+              r1.x += __shfl_xor_sync(0xffffffffu, r1.x, o);
+              r1.y += __shfl_xor_sync(0xffffffffu, r1.y, o);
+            }
+          }
+          if (have_p && lane == 0) {
+            const int32_t blk = d.first_block + lb0 + (SEQ ? pass : 0);
+            if (carried) a.partials[blk].x = r0.x;
+            else a.partials[blk] = r0;
+            if (!SEQ && second) {
+              if (carried) a.partials[blk + 1].x = r1.x;
+              else a.partials[blk + 1] = r1;
+            }
+          }
+        } else {
+          float2 r = make_float2(usq[0] + usq[1], psq[0] + psq[1]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            r.x += __shfl_xor_sync(0xffffffffu, r.x, o);
+            r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
+          }
+          if (G > 1) {
+            r = ring_group_sum2(r, G, warp, lane, sred, parity);
+            parity ^= 1;
+          }
+          if (have_p && j == 0 && lane == 0) {
+            if (carried) a.partials[d.first_block + lb0].x = r.x;
+            else a.partials[d.first_block + lb0] = r;
+          }
+        }
+        continue;
       }
 
       // ---- each block's new absmax (every warp of the group takes part) ----
@@ -853,7 +969,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
     }
   }
 
-  if (a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0) *a.carry_stamp = a.carry_write;
+  if (!NORM && a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0) *a.carry_stamp = a.carry_write;
 
   // ---- a wait ran out: let this warp's copies still in flight land ----
   if (!ok && lane == 0) {
@@ -872,11 +988,11 @@ __host__ __forceinline__ int ring_threads(int log2B) {
   return groups * G * 32;
 }
 
-template <int OPT, int DT, bool WHOLE, bool SEQ>
+template <int OPT, int DT, bool WHOLE, bool SEQ, bool NORM>
 cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   using L = RingSmem<OPT, DT, SEQ>;
   static std::atomic<unsigned char> configured[kMaxDevices];
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SEQ>),
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SEQ, NORM>),
                                       L::kBytes, configured);
   if (e != cudaSuccess) return e;
   const int threads = ring_threads<SEQ>(a.log2B);
@@ -884,19 +1000,19 @@ cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   const int64_t groups = threads / 32 / G;
   const int64_t need = (a.ring_units + groups - 1) / groups;
   const int grid = static_cast<int>(need < a.nsm ? need : a.nsm);
-  k_step8_ring<OPT, DT, WHOLE, SEQ><<<grid, threads, L::kBytes, s>>>(a);
+  k_step8_ring<OPT, DT, WHOLE, SEQ, NORM><<<grid, threads, L::kBytes, s>>>(a);
   return cudaGetLastError();
 }
 
 // Blocksize 256: two passes of a block each (24 warps); larger blocks: one
 // pass over the chunk (16 warps).
-template <int OPT, int DT>
+template <int OPT, int DT, bool NORM>
 cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
   if (a.log2B == 8)
-    return a.whole ? launch_step8_ring_w<OPT, DT, true, true>(a, s)
-                   : launch_step8_ring_w<OPT, DT, false, true>(a, s);
-  return a.whole ? launch_step8_ring_w<OPT, DT, true, false>(a, s)
-                 : launch_step8_ring_w<OPT, DT, false, false>(a, s);
+    return a.whole ? launch_step8_ring_w<OPT, DT, true, true, NORM>(a, s)
+                   : launch_step8_ring_w<OPT, DT, false, true, NORM>(a, s);
+  return a.whole ? launch_step8_ring_w<OPT, DT, true, false, NORM>(a, s)
+                 : launch_step8_ring_w<OPT, DT, false, false, NORM>(a, s);
 }
 
 }  // namespace bnb8
