@@ -629,6 +629,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       uint32_t mx[2][NS];
       float psq[2] = {0.0f, 0.0f};   // sum of p^2 per block half (carried norm; NORM: the old p)
       float usq[2] = {0.0f, 0.0f};   // NORM: sum of u^2 per block half
+      float2 usq2[2] = {f2(0.0f), f2(0.0f)};   // NORM: the same on pairs (whole chunks)
 #pragma unroll
       for (int k = 0; k < NS; ++k) mx[0][k] = mx[1][k] = 0u;
       // the block half of element e of this pass
@@ -636,9 +637,14 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       // element e of this pass is present (partial chunks)
       const bool full = WHOLE || c.v == kChunk;
       auto present = [&](int e) { return full || quad_offset<DT>(lane, q0 + (e >> 2)) + (e & 3) < c.v; };
-      // NORM: one element's direction into its block half's sum
-      auto add_u = [&](int e, float u) {
-        if (present(e)) usq[half_of(e)] = usq[half_of(e)] + u * u;
+      // NORM: the directions of elements e, e + 1 into their block half's sums
+      auto add_u2 = [&](int e, float2 u) {
+        if (full) {
+          usq2[half_of(e)] = fma2(u, u, usq2[half_of(e)]);
+        } else {
+          if (present(e)) usq[half_of(e)] = usq[half_of(e)] + u.x * u.x;
+          if (present(e + 1)) usq[half_of(e)] = usq[half_of(e)] + u.y * u.y;
+        }
       };
       if (have_p) {
         // optimizers whose direction is n / (sqrt(v) + eps)
@@ -695,8 +701,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             const float2 m = fma2(f2(a.b1), stt[0], gg);
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
             if (NORM) {
-              add_u(e, m.x);
-              add_u(e + 1, m.y);
+              add_u2(e, m);
             } else {
               pair_apply<OPT>(a, -eff, pp, m);
               p[e] = pp.x; p[e + 1] = pp.y;
@@ -709,8 +714,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
             if (NORM) {
-              add_u(e, u.x);
-              add_u(e + 1, u.y);
+              add_u2(e, u);
             } else {
               pair_apply<OPT>(a, -eff, pp, u);
               p[e] = pp.x; p[e + 1] = pp.y;
@@ -756,8 +760,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
               if (NORM) {
-                add_u(e, u.x);
-                add_u(e + 1, u.y);
+                add_u2(e, u);
               } else {
                 float2 pp = make_float2(p[e], p[e + 1]);
                 pair_apply<OPT>(a, -eff, pp, u);
@@ -769,8 +772,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
               if (NORM) {
-                add_u(e, u.x);
-                add_u(e + 1, u.y);
+                add_u2(e, u);
               } else {
                 float2 pp = make_float2(p[e], p[e + 1]);
                 pair_apply<OPT>(a, -eff, pp, u);
@@ -782,10 +784,18 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
         if (NORM) {
           // the parameter norm of the step's input (unless carried)
           if (!carried) {
+            float2 psq2[2] = {f2(0.0f), f2(0.0f)};
 #pragma unroll
-            for (int e = 0; e < NE; ++e)
-              if (present(e)) psq[half_of(e)] = psq[half_of(e)] + p[e] * p[e];
+            for (int e = 0; e < NE; e += 2) {
+              // absent elements of a partial chunk hold p = 0
+              const float2 pp = make_float2(p[e], p[e + 1]);
+              psq2[half_of(e)] = fma2(pp, pp, psq2[half_of(e)]);
+            }
+            psq[0] = psq2[0].x + psq2[0].y;
+            psq[1] = psq2[1].x + psq2[1].y;
           }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) usq[h] = usq[h] + (usq2[h].x + usq2[h].y);
         } else {
           ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
         }
