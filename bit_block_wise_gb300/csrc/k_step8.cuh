@@ -563,11 +563,12 @@ cudaError_t launch_step8_skip(const StepArgs& a, int grid, cudaStream_t s) {
 
 template <int OPT, int DT, int MODE>
 cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
-  // the plain step and its max_unorm pre-pass over blocks of 256 elements or
-  // more: the async-copy ring
-  if constexpr (MODE == MODE_STEP || MODE == MODE_NORM) {
+  // the plain step, its max_unorm pre-pass and the step with max_unorm per
+  // block, over blocks of 256 elements or more: the async-copy ring
+  if constexpr (MODE == MODE_STEP || MODE == MODE_NORM || MODE == MODE_BCLIP) {
     if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0)
-      return launch_step8_ring<OPT, DT, MODE == MODE_NORM>(a, s);
+      return launch_step8_ring<OPT, DT, MODE == MODE_STEP ? RING_STEP
+                                        : (MODE == MODE_NORM ? RING_NORM : RING_BCLIP)>(a, s);
   }
   return a.skip_zeros ? launch_step8_skip<OPT, DT, MODE, true>(a, grid, s)
                       : launch_step8_skip<OPT, DT, MODE, false>(a, grid, s);

@@ -405,14 +405,20 @@ __device__ __forceinline__ float2 ring_group_sum2(float2 v, int G, int warp, int
 // multiple of max(512, B) elements, so every chunk is whole and streams
 // through the ring; the element-wise paths for ragged or misaligned chunks are
 // compiled out.  SEQ: blocksize 256, two passes per chunk (RingShape).
-// NORM: the per-tensor max_unorm pre-pass instead of the step: the same
-// update directions u, summed per block as (sum u^2, sum p^2) into
-// StepArgs::partials; nothing else is written.  With a carried norm
-// (BNB8_CARRY_PNORM) the p^2 sums are already there, and p is not even read
-// when the direction does not need it.
-template <int OPT, int DT, bool WHOLE, bool SEQ, bool NORM>
+// RM (ring mode): RING_STEP the step; RING_NORM the per-tensor max_unorm
+// pre-pass: the same update directions u, summed per block as (sum u^2,
+// sum p^2) into StepArgs::partials, nothing else written (with a carried
+// norm, BNB8_CARRY_PNORM, the p^2 sums are already there, and p is not even
+// read when the direction does not need it); RING_BCLIP the step with
+// max_unorm per block: each block's directions are kept until its
+// unorm_c * ||u|| and ||p|| are known, and the block's multiplier scales its
+// step.
+enum RingMode { RING_STEP = 0, RING_NORM = 1, RING_BCLIP = 2 };
+template <int OPT, int DT, bool WHOLE, bool SEQ, int RM>
 __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
     k_step8_ring(const __grid_constant__ StepArgs a) {
+  constexpr bool NORM = RM == RING_NORM;
+  constexpr bool BCLIP = RM == RING_BCLIP;
   using L = RingSmem<OPT, DT, SEQ>;
   using R = RingShape<SEQ>;
   constexpr int NS = L::NS;
@@ -628,8 +634,9 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       float sv[NS][NE];
       uint32_t mx[2][NS];
       float psq[2] = {0.0f, 0.0f};   // sum of p^2 per block half (carried norm; NORM: the old p)
-      float usq[2] = {0.0f, 0.0f};   // NORM: sum of u^2 per block half
-      float2 usq2[2] = {f2(0.0f), f2(0.0f)};   // NORM: the same on pairs (whole chunks)
+      float usq[2] = {0.0f, 0.0f};   // NORM, BCLIP: sum of u^2 per block half
+      float2 usq2[2] = {f2(0.0f), f2(0.0f)};   // NORM, BCLIP: the same on pairs (whole chunks)
+      float ud[BCLIP ? NE : 1];      // BCLIP: the directions, applied once the block's clip is known
 #pragma unroll
       for (int k = 0; k < NS; ++k) mx[0][k] = mx[1][k] = 0u;
       // the block half of element e of this pass
@@ -637,7 +644,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       // element e of this pass is present (partial chunks)
       const bool full = WHOLE || c.v == kChunk;
       auto present = [&](int e) { return full || quad_offset<DT>(lane, q0 + (e >> 2)) + (e & 3) < c.v; };
-      // NORM: the directions of elements e, e + 1 into their block half's sums
+      // NORM, BCLIP: the directions of elements e, e + 1 into their block half's sums
       auto add_u2 = [&](int e, float2 u) {
         if (full) {
           usq2[half_of(e)] = fma2(u, u, usq2[half_of(e)]);
@@ -700,9 +707,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
           } else if (OPT == MOMENTUM) {
             const float2 m = fma2(f2(a.b1), stt[0], gg);
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
-            if (NORM) {
-              add_u2(e, m);
-            } else {
+            if (NORM || BCLIP) add_u2(e, m);
+            if (BCLIP) {
+              ud[e] = m.x; ud[e + 1] = m.y;
+            } else if (!NORM) {
               pair_apply<OPT>(a, -eff, pp, m);
               p[e] = pp.x; p[e + 1] = pp.y;
             }
@@ -713,9 +721,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
             const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
-            if (NORM) {
-              add_u2(e, u);
-            } else {
+            if (NORM || BCLIP) add_u2(e, u);
+            if (BCLIP) {
+              ud[e] = u.x; ud[e + 1] = u.y;
+            } else if (!NORM) {
               pair_apply<OPT>(a, -eff, pp, u);
               p[e] = pp.x; p[e + 1] = pp.y;
             }
@@ -759,9 +768,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              if (NORM) {
-                add_u2(e, u);
-              } else {
+              if (NORM || BCLIP) add_u2(e, u);
+              if (BCLIP) {
+                ud[e] = u.x; ud[e + 1] = u.y;
+              } else if (!NORM) {
                 float2 pp = make_float2(p[e], p[e + 1]);
                 pair_apply<OPT>(a, -eff, pp, u);
                 p[e] = pp.x; p[e + 1] = pp.y;
@@ -771,9 +781,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < NE; e += 2) {
               const float2 u = ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              if (NORM) {
-                add_u2(e, u);
-              } else {
+              if (NORM || BCLIP) add_u2(e, u);
+              if (BCLIP) {
+                ud[e] = u.x; ud[e + 1] = u.y;
+              } else if (!NORM) {
                 float2 pp = make_float2(p[e], p[e + 1]);
                 pair_apply<OPT>(a, -eff, pp, u);
                 p[e] = pp.x; p[e + 1] = pp.y;
@@ -781,7 +792,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
             }
           }
         }
-        if (NORM) {
+        if (NORM || BCLIP) {
           // the parameter norm of the step's input (unless carried)
           if (!carried) {
             float2 psq2[2] = {f2(0.0f), f2(0.0f)};
@@ -796,10 +807,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) usq[h] = usq[h] + (usq2[h].x + usq2[h].y);
-        } else {
-          ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
         }
-        if (!NORM && a.carry_out) {
+        if (RM == RING_STEP)
+          ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
+        if (RM == RING_STEP && a.carry_out) {
           // the squares of p as stored (rounded to the dtype); the registers
           // of a partial chunk's absent elements hold no parameter
 #pragma unroll
@@ -814,6 +825,45 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
         for (int k = 0; k < NS; ++k)
 #pragma unroll
           for (int e = 0; e < NE; ++e) sv[k][e] = 0.0f;
+      }
+
+      if constexpr (BCLIP) {
+        // the block's sums (every lane receives them; every warp of a group
+        // takes part, those without elements with zeros), its multiplier,
+        // the step
+        float2 r0 = make_float2(usq[0], psq[0]), r1 = make_float2(usq[1], psq[1]);
+        if (!SEQ && !two) r0 = make_float2(usq[0] + usq[1], psq[0] + psq[1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          r0.x += __shfl_xor_sync(0xffffffffu, r0.x, o);
+          r0.y += __shfl_xor_sync(0xffffffffu, r0.y, o);
+          if (!SEQ) {
+            r1.x += __shfl_xor_sync(0xffffffffu, r1.x, o);
+            r1.y += __shfl_xor_sync(0xffffffffu, r1.y, o);
+          }
+        }
+        if (!SEQ && !two && G > 1) {
+          r0 = ring_group_sum2(r0, G, warp, lane, sred, parity);
+          parity ^= 1;
+        }
+        if (!SEQ && !two) r1 = r0;
+        if (have_p) {
+          float effb[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 r = h == 0 ? r0 : r1;
+            const float unorm = a.unorm_c * sqrtf(r.x);
+            const float limit = a.max_unorm * sqrtf(r.y);
+            effb[h] = eff * (unorm > limit ? limit / unorm : 1.0f);
+          }
+#pragma unroll
+          for (int e = 0; e < NE; e += 2) {
+            float2 pp = make_float2(p[e], p[e + 1]);
+            pair_apply<OPT>(a, -effb[half_of(e)], pp, make_float2(ud[e], ud[e + 1]));
+            p[e] = pp.x; p[e + 1] = pp.y;
+          }
+          ring_store<DT, NQ>(d.p, c.e0, WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, p);
+        }
       }
 
       if constexpr (NORM) {
@@ -876,7 +926,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < NS; ++k) mx[1][k] = mx[0][k];
       }
-      if (a.carry_out) {
+      if (RM == RING_STEP && a.carry_out) {
         if (SEQ || two) {
           float s0 = psq[0], s1 = psq[1];
 #pragma unroll
@@ -979,7 +1029,8 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
     }
   }
 
-  if (!NORM && a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0) *a.carry_stamp = a.carry_write;
+  if (RM == RING_STEP && a.carry_writer && blockIdx.x == 0 && threadIdx.x == 0)
+    *a.carry_stamp = a.carry_write;
 
   // ---- a wait ran out: let this warp's copies still in flight land ----
   if (!ok && lane == 0) {
@@ -998,11 +1049,11 @@ __host__ __forceinline__ int ring_threads(int log2B) {
   return groups * G * 32;
 }
 
-template <int OPT, int DT, bool WHOLE, bool SEQ, bool NORM>
+template <int OPT, int DT, bool WHOLE, bool SEQ, int RM>
 cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   using L = RingSmem<OPT, DT, SEQ>;
   static std::atomic<unsigned char> configured[kMaxDevices];
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SEQ, NORM>),
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SEQ, RM>),
                                       L::kBytes, configured);
   if (e != cudaSuccess) return e;
   const int threads = ring_threads<SEQ>(a.log2B);
@@ -1010,19 +1061,19 @@ cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   const int64_t groups = threads / 32 / G;
   const int64_t need = (a.ring_units + groups - 1) / groups;
   const int grid = static_cast<int>(need < a.nsm ? need : a.nsm);
-  k_step8_ring<OPT, DT, WHOLE, SEQ, NORM><<<grid, threads, L::kBytes, s>>>(a);
+  k_step8_ring<OPT, DT, WHOLE, SEQ, RM><<<grid, threads, L::kBytes, s>>>(a);
   return cudaGetLastError();
 }
 
 // Blocksize 256: two passes of a block each (24 warps); larger blocks: one
 // pass over the chunk (16 warps).
-template <int OPT, int DT, bool NORM>
+template <int OPT, int DT, int RM>
 cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
   if (a.log2B == 8)
-    return a.whole ? launch_step8_ring_w<OPT, DT, true, true, NORM>(a, s)
-                   : launch_step8_ring_w<OPT, DT, false, true, NORM>(a, s);
-  return a.whole ? launch_step8_ring_w<OPT, DT, true, false, NORM>(a, s)
-                 : launch_step8_ring_w<OPT, DT, false, false, NORM>(a, s);
+    return a.whole ? launch_step8_ring_w<OPT, DT, true, true, RM>(a, s)
+                   : launch_step8_ring_w<OPT, DT, false, true, RM>(a, s);
+  return a.whole ? launch_step8_ring_w<OPT, DT, true, false, RM>(a, s)
+                 : launch_step8_ring_w<OPT, DT, false, false, RM>(a, s);
 }
 
 }  // namespace bnb8
