@@ -89,11 +89,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // geometry and shared memory layout
 // ---------------------------------------------------------------------------
-// A warp takes 512 elements (a chunk) per iteration, in one of two shapes:
-//  SEQ  (blocksize 256): two passes of 8 elements a lane, one block each;
-//       24 warps of up to 80 registers.
-//  !SEQ (blocksize >= 256): one pass of 16 elements a lane; 16 warps of up
-//       to 128 registers.
+// A warp takes 512 elements (a chunk) per iteration, in one of three shapes:
+//  SH_TWO (blocksize 256): two passes of 8 elements a lane, one block each;
+//         24 warps of up to 80 registers.
+//  SH_BIG (blocksize >= 512, where the park fits): two passes of 8 elements
+//         a lane of one block, the first pass's new states parked in shared
+//         memory until the block's absmax is known; 24 warps.
+//  SH_ONE (blocksize >= 512 otherwise): one pass of 16 elements a lane; 16
+//         warps of up to 128 registers.
 // Either way the per-chunk work (the wait, the copies of the next chunk,
 // the chunk's bookkeeping) is paid once per 512 elements.
 constexpr int kChunk = 512;                              // elements per warp and iteration
@@ -105,8 +108,10 @@ struct RingShape {
   static constexpr int kQuads = SEQ ? 2 : 4;             // quads of 4 elements a lane per pass
   static constexpr int kNE = 4 * kQuads;                 // elements a lane per pass
 };
-template <int OPT, int DT, bool SEQ>
+enum RingShapeId { SH_ONE = 0, SH_TWO = 1, SH_BIG = 2 };
+template <int OPT, int DT, int SH>
 struct RingSmem {
+  static constexpr bool SEQ = SH != SH_ONE;
   static constexpr int NS = Traits<OPT>::NS;
   static constexpr int NM = Traits<OPT>::NM;
   static constexpr int ES = DT == DT_F32 ? 4 : 2;
@@ -136,7 +141,15 @@ struct RingSmem {
   static constexpr int kStages = kRing + kWarps * 2 * (kStage + 8) <= kBudget ? 2 : 1;
   static_assert(kRing + kWarps * kStages * (kStage + 8) <= kBudget, "the ring fits");
   static constexpr int kBars = kRing + kWarps * kStages * kStage;
-  static constexpr int kBytes = kBars + kWarps * kStages * 8;
+  // SEQ with blocks of 512 or more: each warp parks its first pass's new
+  // states (NS x 256 floats) until the block's absmax is known; offered only
+  // where the park fits beside the same number of stages
+  static constexpr int kParkWarp = NS * 256 * 4;
+  static constexpr bool kPark =
+      SH == SH_BIG && NS <= 2 && kRing + kWarps * (kStages * (kStage + 8) + kParkWarp) <= kBudget;
+  static constexpr int kPark0 = kBars + kWarps * kStages * 8;
+  static_assert(kPark0 % 16 == 0, "the park keeps 16-byte alignment");
+  static constexpr int kBytes = kPark0 + (kPark ? kWarps * kParkWarp : 0);
 };
 
 // ---------------------------------------------------------------------------
@@ -404,7 +417,7 @@ __device__ __forceinline__ float2 ring_group_sum2(float2 v, int G, int warp, int
 // WHOLE: every tensor of the launch is aligned for bulk copies and a
 // multiple of max(512, B) elements, so every chunk is whole and streams
 // through the ring; the element-wise paths for ragged or misaligned chunks are
-// compiled out.  SEQ: blocksize 256, two passes per chunk (RingShape).
+// compiled out.  SH: the shape (RingShapeId).
 // RM (ring mode): RING_STEP the step; RING_NORM the per-tensor max_unorm
 // pre-pass: the same update directions u, summed per block as (sum u^2,
 // sum p^2) into StepArgs::partials, nothing else written (with a carried
@@ -414,12 +427,14 @@ __device__ __forceinline__ float2 ring_group_sum2(float2 v, int G, int warp, int
 // unorm_c * ||u|| and ||p|| are known, and the block's multiplier scales its
 // step.
 enum RingMode { RING_STEP = 0, RING_NORM = 1, RING_BCLIP = 2 };
-template <int OPT, int DT, bool WHOLE, bool SEQ, int RM>
-__global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
+template <int OPT, int DT, bool WHOLE, int SH, int RM>
+__global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
     k_step8_ring(const __grid_constant__ StepArgs a) {
   constexpr bool NORM = RM == RING_NORM;
   constexpr bool BCLIP = RM == RING_BCLIP;
-  using L = RingSmem<OPT, DT, SEQ>;
+  constexpr bool SEQ = SH != SH_ONE;
+  constexpr bool BIG = SH == SH_BIG;
+  using L = RingSmem<OPT, DT, SH>;
   using R = RingShape<SEQ>;
   constexpr int NS = L::NS;
   constexpr int NM = L::NM;
@@ -440,11 +455,12 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   unsigned char* ring = smem + L::kRing + warp * kStages * L::kStage;
+  float* park = reinterpret_cast<float*>(smem + L::kPark0) + warp * (L::kParkWarp / 4);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars) + warp * kStages;
 
   // ---- geometry: groups of G warps share a unit ----
-  const bool two = SEQ || a.log2B == 8;                    // two blocks per chunk
-  const int G = (!SEQ && a.log2B > kLog2Chunk) ? (1 << (a.log2B - kLog2Chunk)) : 1;
+  const bool two = SH == SH_TWO || (SH == SH_ONE && a.log2B == 8);   // two blocks per chunk
+  const int G = a.log2B > kLog2Chunk ? (1 << (a.log2B - kLog2Chunk)) : 1;
   const int nwarps = static_cast<int>(blockDim.x >> 5);   // a multiple of G (host)
   const int gpc = nwarps / G;                              // groups per CTA
   const int j = warp % G;                                  // chunk of the unit
@@ -539,8 +555,9 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
     }
     const DevTensor& d = a.t[c.t];
     const int32_t lb0 = chunk_block(two, c.u, 0);
-    // the chunk's second block exists (two blocks per chunk, more than 256 present)
-    const bool second = two && c.v > 256;
+    // the chunk's second half has elements (and, B = 256, is a second block)
+    const bool half1 = WHOLE || c.v > 256;
+    const bool second = two && half1;
     const bool have = (WHOLE || c.v > 0) && ok;   // (before this chunk's wait)
     bool staged = false;     // the chunk is in stage s (else read from global memory)
     if ((want >> s) & 1u) {
@@ -577,12 +594,92 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       }
     };
     const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
+    // SEQ, blocks of 512 or more: the block's lane maxima and sums over both passes
+    uint32_t mxc[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) mxc[k] = 0u;
+    float usq_c = 0.0f, psq_c = 0.0f;
+
+    // requantize the lane's new states svx of quads q0x.. with the block
+    // absmax mxh (per block half) and store their codes.  The usual case:
+    // every state's absmax lies in [2^-125, 2^125] (or is 0, an all-zero
+    // block) and every map takes the table: one Newton reciprocal per block
+    // and state and the table lookups, no other tests.
+    auto encode_store = [&](const float (&svx)[NS][NE], int q0x, const uint32_t (&mxh)[2][NS]) {
+      constexpr int NH = SEQ ? 1 : 2;   // block halves of a pass
+      auto hf = [](int e) { return SEQ ? 0 : (e >> 3); };
+      uint32_t enc[NS][NE];
+      bool usual = true;
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        const int m = Traits<OPT>::map_of(k);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          usual = usual && (mxh[h][k] - 0x01000000u <= 0x7D000000u || mxh[h][k] == 0u);
+        usual = usual && fast_map[m] && (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
+      }
+      if (usual) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          float inv[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float amk = __uint_as_float(mxh[h][k]);
+            const float y = rcp_approx(amk);
+            const float r = __fmaf_rn(__fmaf_rn(-amk, y, 1.0f), y, y);
+            inv[h] = mxh[h][k] == 0u ? 0.0f : r;
+          }
+          const uint32_t* tz = stbl + Traits<OPT>::map_of(k) * kTblSize + kTblZero;
+#pragma unroll
+          for (int e = 0; e < NE; e += 2) {
+            const float2 xn = mul2(make_float2(svx[k][e], svx[k][e + 1]), f2(inv[hf(e)]));
+            if (Traits<OPT>::nonneg(k)) {
+              enc[k][e] = encode_xn_nonneg(xn.x, tz);
+              enc[k][e + 1] = encode_xn_nonneg(xn.y, tz);
+            } else {
+              enc[k][e] = encode_xn(xn.x, tz);
+              enc[k][e + 1] = encode_xn(xn.y, tz);
+            }
+          }
+        }
+      } else {
+        // absmax tiny, huge or not finite, or a map the table cannot take
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          const int m = Traits<OPT>::map_of(k);
+          const uint32_t* tz = stbl + m * kTblSize + kTblZero;
+          const float* md = smid + m * 256;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float inv = rcp_block(__uint_as_float(mxh[h][k]));
+            const bool fast = fast_map[m] && mxh[h][k] <= 0x7f7fffffu && inv <= FLT_MAX;
+#pragma unroll
+            for (int e = 8 * h; e < 8 * h + 8; ++e) {
+              if (!fast) enc[k][e] = encode_search(svx[k][e] * inv, md);
+              else if (Traits<OPT>::nonneg(k) && nonneg_map[m]) enc[k][e] = encode_fast_nonneg(svx[k][e], inv, tz);
+              else enc[k][e] = encode_fast(svx[k][e], inv, tz);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        // byte 2 of each entry is the code
+        uint32_t w[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i)
+          w[i] = __byte_perm(__byte_perm(enc[k][4 * i], enc[k][4 * i + 1], 0x0062u),
+                             __byte_perm(enc[k][4 * i + 2], enc[k][4 * i + 3], 0x0062u), 0x5410u);
+        ring_store_codes<DT, NQ>(const_cast<uint8_t*>(code_stream<OPT>(d, k)), c.e0,
+                                 WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0x, w);
+      }
+    };
 
 #pragma unroll
     for (int pass = 0; pass < R::kPasses; ++pass) {
       const int q0 = pass * NQ;            // first quad of the pass
       // pass h of SEQ covers block lb0 + h; !SEQ covers the chunk's blocks at once
-      const bool have_p = have && ok && (!SEQ || pass == 0 || second || WHOLE);
+      const bool have_p = have && ok && (!SEQ || pass == 0 || half1);
       float am[2][NS];       // absmax of the blocks of the pass's elements (halves 0, 1)
       float p[NE], g[NE];
       uint32_t cw[NS][NQ];
@@ -600,7 +697,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
           if (SEQ) {
-            am[0][k] = am[1][k] = sa[pass * NS + k];
+            am[0][k] = am[1][k] = sa[(two ? pass : 0) * NS + k];
           } else {
             am[0][k] = sa[k];
             am[1][k] = two ? sa[NS + k] : sa[k];
@@ -610,7 +707,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
           if (SEQ) {
-            am[0][k] = am[1][k] = absmax_stream<OPT>(d, k)[lb0 + pass];
+            am[0][k] = am[1][k] = absmax_stream<OPT>(d, k)[lb0 + (two ? pass : 0)];
           } else {
             am[0][k] = absmax_stream<OPT>(d, k)[lb0];
             am[1][k] = second ? absmax_stream<OPT>(d, k)[lb0 + 1] : am[0][k];
@@ -827,6 +924,77 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
           for (int e = 0; e < NE; ++e) sv[k][e] = 0.0f;
       }
 
+      if constexpr (BIG && RM != RING_BCLIP) {
+        {
+          // Blocks of 512 elements or more: both passes belong to one block
+          // (G warps share it).  The first pass parks its new states in
+          // shared memory; after the second the block's absmax and sums are
+          // reduced (every warp of the group takes part) and both passes are
+          // requantized with the block's reciprocal.
+#pragma unroll
+          for (int k = 0; k < NS; ++k) mxc[k] = mxc[k] > mx[0][k] ? mxc[k] : mx[0][k];
+          usq_c = usq_c + usq[0];
+          psq_c = psq_c + psq[0];
+          if (pass == 0) {
+            if (!NORM && have_p) {
+#pragma unroll
+              for (int k = 0; k < NS; ++k)
+#pragma unroll
+                for (int i = 0; i < NE / 4; ++i)
+                  reinterpret_cast<float4*>(park + k * 256)[i * 32 + lane] =
+                      make_float4(sv[k][4 * i], sv[k][4 * i + 1], sv[k][4 * i + 2], sv[k][4 * i + 3]);
+            }
+            continue;
+          }
+          const bool have_blk = have && ok;
+          if constexpr (NORM) {
+            float2 r = make_float2(usq_c, psq_c);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              r.x += __shfl_xor_sync(0xffffffffu, r.x, o);
+              r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
+            }
+            if (G > 1) {
+              r = ring_group_sum2(r, G, warp, lane, sred, parity);
+              parity ^= 1;
+            }
+            if (have_blk && j == 0 && lane == 0) {
+              if (carried) a.partials[d.first_block + lb0].x = r.x;
+              else a.partials[d.first_block + lb0] = r;
+            }
+          } else {
+            if (a.carry_out) {
+              const float bsq = ring_group_sum(psq_c, G, warp, lane, sred, parity);
+              parity ^= 1;
+              if (have_blk && j == 0 && lane == 0)
+                reinterpret_cast<float*>(a.partials + d.first_block + lb0)[1] = bsq;
+            }
+            ring_group_max<NS>(mxc, G, warp, lane, sred, parity);
+            parity ^= 1;
+            if (have_blk) {
+              uint32_t mxh[2][NS];
+#pragma unroll
+              for (int k = 0; k < NS; ++k) mxh[0][k] = mxh[1][k] = mxc[k];
+              if (have_p) encode_store(sv, q0, mxh);
+              // the first pass's states back from the park
+#pragma unroll
+              for (int k = 0; k < NS; ++k)
+#pragma unroll
+                for (int i = 0; i < NE / 4; ++i) {
+                  const float4 v = reinterpret_cast<const float4*>(park + k * 256)[i * 32 + lane];
+                  sv[k][4 * i] = v.x; sv[k][4 * i + 1] = v.y; sv[k][4 * i + 2] = v.z; sv[k][4 * i + 3] = v.w;
+                }
+              encode_store(sv, 0, mxh);
+              if (j == 0 && lane == 0) {
+#pragma unroll
+                for (int k = 0; k < NS; ++k) absmax_stream<OPT>(d, k)[lb0] = __uint_as_float(mxc[k]);
+              }
+            }
+          }
+          continue;
+        }
+      }
+
       if constexpr (BCLIP) {
         // the block's sums (every lane receives them; every warp of a group
         // takes part, those without elements with zeros), its multiplier,
@@ -868,7 +1036,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 
       if constexpr (NORM) {
         // ---- the blocks' (sum u^2, sum p^2) ----
-        if (SEQ || two) {
+        if (two) {
           float2 r0 = make_float2(usq[0], psq[0]), r1 = make_float2(usq[1], psq[1]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
@@ -927,7 +1095,7 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
         for (int k = 0; k < NS; ++k) mx[1][k] = mx[0][k];
       }
       if (RM == RING_STEP && a.carry_out) {
-        if (SEQ || two) {
+        if (two) {
           float s0 = psq[0], s1 = psq[1];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
@@ -949,75 +1117,10 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
       if (!have_p) continue;
 
       // ---- requantize and store codes (and, once per block, the absmax) ----
-      // The usual case: every state's absmax lies in [2^-125, 2^125] (or is
-      // 0, an all-zero block) and every map takes the table: one Newton
-      // reciprocal per block and state and the table lookups, no other tests.
-      constexpr int NH = SEQ ? 1 : 2;   // block halves of the pass
-      uint32_t enc[NS][NE];
-      bool usual = true;
-#pragma unroll
-      for (int k = 0; k < NS; ++k) {
-        const int m = Traits<OPT>::map_of(k);
-#pragma unroll
-        for (int h = 0; h < NH; ++h)
-          usual = usual && (mx[h][k] - 0x01000000u <= 0x7D000000u || mx[h][k] == 0u);
-        usual = usual && fast_map[m] && (!Traits<OPT>::nonneg(k) || nonneg_map[m]);
-      }
-      if (usual) {
+      encode_store(sv, q0, mx);
+      if (j == 0 && lane == 0) {
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
-          float inv[NH];
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const float amk = __uint_as_float(mx[h][k]);
-            const float y = rcp_approx(amk);
-            const float r = __fmaf_rn(__fmaf_rn(-amk, y, 1.0f), y, y);
-            inv[h] = mx[h][k] == 0u ? 0.0f : r;
-          }
-          const uint32_t* tz = stbl + Traits<OPT>::map_of(k) * kTblSize + kTblZero;
-#pragma unroll
-          for (int e = 0; e < NE; e += 2) {
-            const float2 xn = mul2(make_float2(sv[k][e], sv[k][e + 1]), f2(inv[half_of(e)]));
-            if (Traits<OPT>::nonneg(k)) {
-              enc[k][e] = encode_xn_nonneg(xn.x, tz);
-              enc[k][e + 1] = encode_xn_nonneg(xn.y, tz);
-            } else {
-              enc[k][e] = encode_xn(xn.x, tz);
-              enc[k][e + 1] = encode_xn(xn.y, tz);
-            }
-          }
-        }
-      } else {
-        // absmax tiny, huge or not finite, or a map the table cannot take
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-          const int m = Traits<OPT>::map_of(k);
-          const uint32_t* tz = stbl + m * kTblSize + kTblZero;
-          const float* md = smid + m * 256;
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const float inv = rcp_block(__uint_as_float(mx[h][k]));
-            const bool fast = fast_map[m] && mx[h][k] <= 0x7f7fffffu && inv <= FLT_MAX;
-#pragma unroll
-            for (int e = 8 * h; e < 8 * h + 8; ++e) {
-              if (!fast) enc[k][e] = encode_search(sv[k][e] * inv, md);
-              else if (Traits<OPT>::nonneg(k) && nonneg_map[m]) enc[k][e] = encode_fast_nonneg(sv[k][e], inv, tz);
-              else enc[k][e] = encode_fast(sv[k][e], inv, tz);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < NS; ++k) {
-        // byte 2 of each entry is the code
-        uint32_t w[NQ];
-#pragma unroll
-        for (int i = 0; i < NQ; ++i)
-          w[i] = __byte_perm(__byte_perm(enc[k][4 * i], enc[k][4 * i + 1], 0x0062u),
-                             __byte_perm(enc[k][4 * i + 2], enc[k][4 * i + 3], 0x0062u), 0x5410u);
-        ring_store_codes<DT, NQ>(const_cast<uint8_t*>(code_stream<OPT>(d, k)), c.e0,
-                                 WHOLE ? kChunk : c.v, WHOLE || (d.vec_ok & 1) != 0, lane, q0, w);
-        if (j == 0 && lane == 0) {
           if (SEQ) {
             absmax_stream<OPT>(d, k)[lb0 + pass] = __uint_as_float(mx[0][k]);
           } else {
@@ -1041,39 +1144,46 @@ __global__ void __launch_bounds__(RingShape<SEQ>::kWarps * 32, 1)
 
 // CTA size for a launch: as many warps as the ring holds, whole groups.
 // (at most 15 groups: named barriers 1..15 are the groups' meeting points)
-template <bool SEQ>
+template <int SH>
 __host__ __forceinline__ int ring_threads(int log2B) {
-  const int G = (!SEQ && log2B > kLog2Chunk) ? (1 << (log2B - kLog2Chunk)) : 1;
+  constexpr bool SEQ = SH != SH_ONE;
+  const int G = log2B > kLog2Chunk ? (1 << (log2B - kLog2Chunk)) : 1;
   int groups = RingShape<SEQ>::kWarps / G;
   if (G > 1 && groups > 15) groups = 15;
   return groups * G * 32;
 }
 
-template <int OPT, int DT, bool WHOLE, bool SEQ, int RM>
+template <int OPT, int DT, bool WHOLE, int SH, int RM>
 cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
-  using L = RingSmem<OPT, DT, SEQ>;
+  using L = RingSmem<OPT, DT, SH>;
   static std::atomic<unsigned char> configured[kMaxDevices];
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SEQ, RM>),
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SH, RM>),
                                       L::kBytes, configured);
   if (e != cudaSuccess) return e;
-  const int threads = ring_threads<SEQ>(a.log2B);
-  const int G = (!SEQ && a.log2B > kLog2Chunk) ? (1 << (a.log2B - kLog2Chunk)) : 1;
+  const int threads = ring_threads<SH>(a.log2B);
+  const int G = a.log2B > kLog2Chunk ? (1 << (a.log2B - kLog2Chunk)) : 1;
   const int64_t groups = threads / 32 / G;
   const int64_t need = (a.ring_units + groups - 1) / groups;
   const int grid = static_cast<int>(need < a.nsm ? need : a.nsm);
-  k_step8_ring<OPT, DT, WHOLE, SEQ, RM><<<grid, threads, L::kBytes, s>>>(a);
+  k_step8_ring<OPT, DT, WHOLE, SH, RM><<<grid, threads, L::kBytes, s>>>(a);
   return cudaGetLastError();
 }
 
-// Blocksize 256: two passes of a block each (24 warps); larger blocks: one
-// pass over the chunk (16 warps).
+// Blocksize 256: two passes of a block each (24 warps); larger blocks: two
+// passes of one block with the first pass parked (24 warps) where the park
+// fits, else one pass over the chunk (16 warps).
 template <int OPT, int DT, int RM>
 cudaError_t launch_step8_ring(const StepArgs& a, cudaStream_t s) {
   if (a.log2B == 8)
-    return a.whole ? launch_step8_ring_w<OPT, DT, true, true, RM>(a, s)
-                   : launch_step8_ring_w<OPT, DT, false, true, RM>(a, s);
-  return a.whole ? launch_step8_ring_w<OPT, DT, true, false, RM>(a, s)
-                 : launch_step8_ring_w<OPT, DT, false, false, RM>(a, s);
+    return a.whole ? launch_step8_ring_w<OPT, DT, true, SH_TWO, RM>(a, s)
+                   : launch_step8_ring_w<OPT, DT, false, SH_TWO, RM>(a, s);
+  if constexpr (RM != RING_BCLIP && RingSmem<OPT, DT, SH_BIG>::kPark) {
+    return a.whole ? launch_step8_ring_w<OPT, DT, true, SH_BIG, RM>(a, s)
+                   : launch_step8_ring_w<OPT, DT, false, SH_BIG, RM>(a, s);
+  } else {
+    return a.whole ? launch_step8_ring_w<OPT, DT, true, SH_ONE, RM>(a, s)
+                   : launch_step8_ring_w<OPT, DT, false, SH_ONE, RM>(a, s);
+  }
 }
 
 }  // namespace bnb8
