@@ -515,7 +515,13 @@ def run_gpu(args, wl):
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dist_ms = step_distribution(per_step)
     ms_per_step = max_over_ranks(dist_ms["median"], world, device)
-    n_chunks8 = -(-sum(1 for b in wl.bits if b == 8) // 96)
+    # the library's plan: at most 96 tensors per launch; 8-bit tensors that
+    # are multiples of max(512, B) elements launch apart from the others
+    # (every tensor here is 256-byte aligned)
+    unit = max(512, wl.blocksize)
+    whole8 = sum(1 for n, b in zip(wl.sizes, wl.bits) if b == 8 and n % unit == 0)
+    rest8 = sum(1 for b in wl.bits if b == 8) - whole8
+    n_chunks8 = -(-whole8 // 96) + -(-rest8 // 96)
     n_chunks32 = -(-sum(1 for b in wl.bits if b == 32) // 96)
     launches_per_step = n_chunks8 + n_chunks32
     if wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block"):

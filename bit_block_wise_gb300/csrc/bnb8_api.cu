@@ -229,26 +229,34 @@ int make_plan(const bnb8_tensor* ts, int nt, const bnb8_hparams& hp, int log2B,
     if (!aligned(qmap1, 4) || (qmap2 != nullptr && !aligned(qmap2, 4)))
       return fail(BNB8_EINVAL, "qmaps must be 4-byte aligned");
   }
+  // 8-bit tensors whose chunks are all whole for the ring step (aligned, a
+  // multiple of max(512, B) elements) are launched apart from the others,
+  // so that their launches take the ring's whole-chunk variant
+  const int64_t unit = int64_t(1) << (log2B > 9 ? log2B : 9);
+  auto whole = [&](int i) { return plan->vec[i] == 3 && ts[i].n % unit == 0; };
   int64_t offset = 0;
   for (int bits : {8, 32}) {
-    Plan::Chunk cur;
-    cur.bits = bits;
-    for (int i = 0; i < nt; ++i) {
-      if (ts[i].n == 0 || ts[i].state_bits != bits) continue;
-      if (static_cast<int>(cur.idx.size()) == kMaxTensors) {
+    for (int group = 0; group < (bits == 8 ? 2 : 1); ++group) {
+      Plan::Chunk cur;
+      cur.bits = bits;
+      for (int i = 0; i < nt; ++i) {
+        if (ts[i].n == 0 || ts[i].state_bits != bits) continue;
+        if (bits == 8 && whole(i) != (group == 0)) continue;
+        if (static_cast<int>(cur.idx.size()) == kMaxTensors) {
+          cur.partial_offset = offset;
+          offset += cur.total_blocks;
+          plan->chunks.push_back(cur);
+          cur = Plan::Chunk();
+          cur.bits = bits;
+        }
+        cur.idx.push_back(i);
+        cur.total_blocks += (ts[i].n + (int64_t(1) << log2B) - 1) >> log2B;
+      }
+      if (!cur.idx.empty()) {
         cur.partial_offset = offset;
         offset += cur.total_blocks;
         plan->chunks.push_back(cur);
-        cur = Plan::Chunk();
-        cur.bits = bits;
       }
-      cur.idx.push_back(i);
-      cur.total_blocks += (ts[i].n + (int64_t(1) << log2B) - 1) >> log2B;
-    }
-    if (!cur.idx.empty()) {
-      cur.partial_offset = offset;
-      offset += cur.total_blocks;
-      plan->chunks.push_back(cur);
     }
   }
   plan->all_blocks = offset;

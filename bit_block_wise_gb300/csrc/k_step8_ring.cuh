@@ -925,74 +925,72 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
       }
 
       if constexpr (BIG && RM != RING_BCLIP) {
-        {
-          // Blocks of 512 elements or more: both passes belong to one block
-          // (G warps share it).  The first pass parks its new states in
-          // shared memory; after the second the block's absmax and sums are
-          // reduced (every warp of the group takes part) and both passes are
-          // requantized with the block's reciprocal.
+        // Blocks of 512 elements or more: both passes belong to one block
+        // (G warps share it).  The first pass parks its new states in
+        // shared memory; after the second the block's absmax and sums are
+        // reduced (every warp of the group takes part) and both passes are
+        // requantized with the block's reciprocal.
 #pragma unroll
-          for (int k = 0; k < NS; ++k) mxc[k] = mxc[k] > mx[0][k] ? mxc[k] : mx[0][k];
-          usq_c = usq_c + usq[0];
-          psq_c = psq_c + psq[0];
-          if (pass == 0) {
-            if (!NORM && have_p) {
+        for (int k = 0; k < NS; ++k) mxc[k] = mxc[k] > mx[0][k] ? mxc[k] : mx[0][k];
+        usq_c = usq_c + usq[0];
+        psq_c = psq_c + psq[0];
+        if (pass == 0) {
+          if (!NORM && have_p) {
 #pragma unroll
-              for (int k = 0; k < NS; ++k)
+            for (int k = 0; k < NS; ++k)
 #pragma unroll
-                for (int i = 0; i < NE / 4; ++i)
-                  reinterpret_cast<float4*>(park + k * 256)[i * 32 + lane] =
-                      make_float4(sv[k][4 * i], sv[k][4 * i + 1], sv[k][4 * i + 2], sv[k][4 * i + 3]);
-            }
-            continue;
-          }
-          const bool have_blk = have && ok;
-          if constexpr (NORM) {
-            float2 r = make_float2(usq_c, psq_c);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              r.x += __shfl_xor_sync(0xffffffffu, r.x, o);
-              r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
-            }
-            if (G > 1) {
-              r = ring_group_sum2(r, G, warp, lane, sred, parity);
-              parity ^= 1;
-            }
-            if (have_blk && j == 0 && lane == 0) {
-              if (carried) a.partials[d.first_block + lb0].x = r.x;
-              else a.partials[d.first_block + lb0] = r;
-            }
-          } else {
-            if (a.carry_out) {
-              const float bsq = ring_group_sum(psq_c, G, warp, lane, sred, parity);
-              parity ^= 1;
-              if (have_blk && j == 0 && lane == 0)
-                reinterpret_cast<float*>(a.partials + d.first_block + lb0)[1] = bsq;
-            }
-            ring_group_max<NS>(mxc, G, warp, lane, sred, parity);
-            parity ^= 1;
-            if (have_blk) {
-              uint32_t mxh[2][NS];
-#pragma unroll
-              for (int k = 0; k < NS; ++k) mxh[0][k] = mxh[1][k] = mxc[k];
-              if (have_p) encode_store(sv, q0, mxh);
-              // the first pass's states back from the park
-#pragma unroll
-              for (int k = 0; k < NS; ++k)
-#pragma unroll
-                for (int i = 0; i < NE / 4; ++i) {
-                  const float4 v = reinterpret_cast<const float4*>(park + k * 256)[i * 32 + lane];
-                  sv[k][4 * i] = v.x; sv[k][4 * i + 1] = v.y; sv[k][4 * i + 2] = v.z; sv[k][4 * i + 3] = v.w;
-                }
-              encode_store(sv, 0, mxh);
-              if (j == 0 && lane == 0) {
-#pragma unroll
-                for (int k = 0; k < NS; ++k) absmax_stream<OPT>(d, k)[lb0] = __uint_as_float(mxc[k]);
-              }
-            }
+              for (int i = 0; i < NE / 4; ++i)
+                reinterpret_cast<float4*>(park + k * 256)[i * 32 + lane] =
+                    make_float4(sv[k][4 * i], sv[k][4 * i + 1], sv[k][4 * i + 2], sv[k][4 * i + 3]);
           }
           continue;
         }
+        const bool have_blk = have && ok;
+        if constexpr (NORM) {
+          float2 r = make_float2(usq_c, psq_c);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            r.x += __shfl_xor_sync(0xffffffffu, r.x, o);
+            r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
+          }
+          if (G > 1) {
+            r = ring_group_sum2(r, G, warp, lane, sred, parity);
+            parity ^= 1;
+          }
+          if (have_blk && j == 0 && lane == 0) {
+            if (carried) a.partials[d.first_block + lb0].x = r.x;
+            else a.partials[d.first_block + lb0] = r;
+          }
+        } else {
+          if (a.carry_out) {
+            const float bsq = ring_group_sum(psq_c, G, warp, lane, sred, parity);
+            parity ^= 1;
+            if (have_blk && j == 0 && lane == 0)
+              reinterpret_cast<float*>(a.partials + d.first_block + lb0)[1] = bsq;
+          }
+          ring_group_max<NS>(mxc, G, warp, lane, sred, parity);
+          parity ^= 1;
+          if (have_blk) {
+            uint32_t mxh[2][NS];
+#pragma unroll
+            for (int k = 0; k < NS; ++k) mxh[0][k] = mxh[1][k] = mxc[k];
+            if (have_p) encode_store(sv, q0, mxh);
+            // the first pass's states back from the park
+#pragma unroll
+            for (int k = 0; k < NS; ++k)
+#pragma unroll
+              for (int i = 0; i < NE / 4; ++i) {
+                const float4 v = reinterpret_cast<const float4*>(park + k * 256)[i * 32 + lane];
+                sv[k][4 * i] = v.x; sv[k][4 * i + 1] = v.y; sv[k][4 * i + 2] = v.z; sv[k][4 * i + 3] = v.w;
+              }
+            encode_store(sv, 0, mxh);
+            if (j == 0 && lane == 0) {
+#pragma unroll
+              for (int k = 0; k < NS; ++k) absmax_stream<OPT>(d, k)[lb0] = __uint_as_float(mxc[k]);
+            }
+          }
+        }
+        continue;
       }
 
       if constexpr (BCLIP) {
