@@ -77,6 +77,9 @@ CASES = [
     ("momentum", "f32", [3000, 128 * 40 + 1], [8, 8], 128, 0.0),
     ("ademamix", "f32", [4096 + 256, 1000], [8, 32], 256, 1e-2),
     ("rmsprop", "f16", [5000, 2600], [8, 8], 256, 0.0),
+    # fp32 blocks of 512 and more: the two-pass shape with the first pass parked
+    ("adam", "f32", [2048 * 3 + 5, 4096], [8, 8], 2048, 1e-2),
+    ("adamw", "f32", [512 * 7 + 100, 1024, 300], [8, 8, 32], 512, 1e-2),
 ]
 
 

@@ -277,26 +277,41 @@ def test_step_max_unorm(bnb8, qdev, optim, dtype):
              max_unorm=0.05, wd=1e-2, seed=6)
 
 
+@pytest.mark.parametrize("optim", ["adam", "lion"])
+@pytest.mark.parametrize("max_unorm", [0.0, 0.05])
+def test_step_list_of_whole_and_ragged_tensors(bnb8, qdev, optim, max_unorm):
+    # the planner launches whole-chunk tensors apart from the ragged ones and
+    # 32-bit tensors apart from both: results and per-tensor multipliers must
+    # not depend on that grouping
+    sizes = [512 * 4, 1000, 512 * 9, 300, 777, 512 * 2, 256 * 3, 4096]
+    bits = [8, 8, 8, 32, 8, 8, 8, 32]
+    run_case(bnb8, qdev, optim, "f32", bits, 256, sizes, steps=2, max_unorm=max_unorm, wd=1e-2,
+             seed=17)
+
+
 @pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
-def test_unorm_scales_match_oracle(bnb8, qdev, optim):
+@pytest.mark.parametrize("B", [256, 2048])
+def test_unorm_scales_match_oracle(bnb8, qdev, optim, B):
+    # B = 2048: the pre-pass's two-pass shape (fp32, <= 2 states) or its
+    # one-pass shape (AdEMAMix), four warps per block, a ragged last block
     q1, q2 = map_pair(optim, S, U)
     sizes, bits = [5000, 700, 256 * 40 + 3], [8, 32, 8]
     params, refs = [], []
     for i, n in enumerate(sizes):
         p = workloads.normal(n, 0.02, 70 + i)
-        st = random_state(optim, n, bits[i], 256, 80 + i, q1, q2)
+        st = random_state(optim, n, bits[i], B, 80 + i, q1, q2)
         refs.append(oracle.TensorState(p.copy(), *st, bits[i]))
         params.append(bnb8.ParamState(to_dev(p), to_dev(workloads.normal(n, 1e-2, 90 + i)),
                                       *[to_dev(a) for a in st], bits[i]))
     hp = dict(HP_BASE[optim], max_unorm=0.02, step=4)
     qd1 = qdev[0] if q1 is S else qdev[1]
-    scales = bnb8.bnb8_unorm(params, bnb8.HParams(optim=optim, **hp), qd1,
+    scales = bnb8.bnb8_unorm(params, bnb8.HParams(optim=optim, blocksize=B, **hp), qd1,
                              None if q2 is None else qdev[1])
     torch.cuda.synchronize()
     got = to_host(scales)
     for i, (ps, r) in enumerate(zip(params, refs)):
         want, unorm, pnorm = oracle.unorm_scale(oracle.HParams(optim=optim, **hp), r,
-                                                to_host(ps.g), "f32", 256, q1, q2)
+                                                to_host(ps.g), "f32", B, q1, q2)
         assert abs(got[i] - want) <= 1e-6 * want, (i, got[i], want)
         assert got[i] < 1.0
 
