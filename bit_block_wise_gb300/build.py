@@ -22,7 +22,8 @@ OPTIMIZERS = ["adam", "adamw", "momentum", "rmsprop", "adagrad", "lion", "ademam
 UNITS = [("bnb8_api.cu", "bnb8_api.o", []), ("k_quant.cu", "k_quant.o", [])] + [
     ("k_step_opt.cu", f"k_step_{name}.o", [f"-DBNB8_OPT={i}"]) for i, name in enumerate(OPTIMIZERS)]
 SOURCES = sorted({src for src, _, _ in UNITS})
-HEADERS = ["bnb8_internal.h", "bnb8_device.cuh", "k_step8.cuh", "k_step8_ring.cuh", "k_step32.cuh"]
+HEADERS = ["bnb8_internal.h", "bnb8_device.cuh", "k_step8.cuh", "k_step8_ring.cuh",
+           "k_step8_ring_skip.cuh", "k_step32.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

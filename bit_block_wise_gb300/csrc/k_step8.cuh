@@ -16,6 +16,7 @@
 
 #include "bnb8_device.cuh"
 #include "k_step8_ring.cuh"
+#include "k_step8_ring_skip.cuh"
 
 namespace bnb8 {
 
@@ -565,6 +566,11 @@ template <int OPT, int DT, int MODE>
 cudaError_t launch_step8_t(const StepArgs& a, int grid, cudaStream_t s) {
   // the plain step, its max_unorm pre-pass and the step with max_unorm per
   // block, over blocks of 256 elements or more: the async-copy ring
+  if constexpr (MODE == MODE_STEP) {
+    // skip_zeros over blocks of 256: the gradient streams through the ring,
+    // live blocks fetch the rest
+    if (a.skip_zeros && a.log2B == 8 && a.tensorwise == 0) return launch_step8_skip_ring<OPT, DT>(a, s);
+  }
   if constexpr (MODE == MODE_STEP || MODE == MODE_NORM || MODE == MODE_BCLIP) {
     if (!a.skip_zeros && a.log2B >= 8 && a.tensorwise == 0)
       return launch_step8_ring<OPT, DT, MODE == MODE_STEP ? RING_STEP

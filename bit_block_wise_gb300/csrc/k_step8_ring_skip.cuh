@@ -1,0 +1,441 @@
+// k_step8_ring_skip.cuh -- the 8-bit step with skip_zeros on a per-warp ring
+// (blocksize 256).
+//
+// skip_zeros ("Support skip_zeros in the XPU Triton optimizer kernels
+// #2097"): an element whose raw gradient is exactly zero keeps its parameter
+// and state; a block whose gradient is all zero is not touched at all.  On
+// sparse gradients (an embedding whose rows are mostly zero) most blocks are
+// such blocks, so the step is a stream of g with a few live blocks in it.
+//
+// Here every warp streams the gradient of its 512-element chunks through a
+// ring of shared-memory stages (bulk copies, as in k_step8_ring, but of g
+// alone, so the ring holds several chunks ahead).  A chunk with a nonzero
+// gradient in either of its two blocks then fetches its p, codes and absmax
+// into the warp's own live buffer (bulk copies on a second mbarrier, one
+// round trip per chunk), and its live blocks are stepped and requantized
+// exactly as in the plain step, with the skipped elements' old parameter and
+// dequantized states kept.  Blocks with an all-zero gradient cost a
+// shared-memory read and a warp vote.
+#pragma once
+
+#include "k_step8_ring.cuh"
+
+namespace bnb8 {
+
+template <int OPT, int DT>
+struct SkipSmem {
+  static constexpr int NS = Traits<OPT>::NS;
+  static constexpr int NM = Traits<OPT>::NM;
+  static constexpr int ES = DT == DT_F32 ? 4 : 2;
+  static constexpr int kWarps = 24;
+  // one stage: g of a chunk | header
+  static constexpr int kSG = 0;
+  static constexpr int kSH = kChunk * ES;
+  static constexpr int kStage = kSH + 16;
+  // the warp's live buffer: a chunk's p | codes of each state | absmax [block][state]
+  static constexpr int kLP = 0;
+  static constexpr int kLC = kChunk * ES;
+  static constexpr int kLA = kLC + NS * kChunk;
+  static constexpr int kLive = kLA + 32;
+  static_assert(2 * NS * 4 <= 32, "absmax slots of two blocks");
+  static_assert(kStage % 16 == 0 && kLive % 16 == 0, "16-byte alignment");
+  // CTA layout: maps, midpoints, bucket tables, rings, stage barriers, live
+  // buffers, live barriers
+  static constexpr int kQ = 0;
+  static constexpr int kMid = kQ + NM * 256 * 4;
+  static constexpr int kTbl = kMid + NM * 256 * 4;
+  static constexpr int kRing = kTbl + NM * kTblSize * 4;
+  static constexpr int kBudget = 232448 - 1024;
+  static constexpr int per_warp(int s) { return s * (kStage + 8) + kLive + 8; }
+  // as many stages (up to 4) as fit: the ring runs that many chunks ahead
+  static constexpr int kStages = kRing + kWarps * per_warp(4) <= kBudget   ? 4
+                                 : kRing + kWarps * per_warp(3) <= kBudget ? 3
+                                 : kRing + kWarps * per_warp(2) <= kBudget ? 2
+                                                                           : 1;
+  static_assert(kRing + kWarps * per_warp(kStages) <= kBudget, "the ring fits");
+  static constexpr int kBars = kRing + kWarps * kStages * kStage;
+  static constexpr int kLive0 = kBars + kWarps * kStages * 8;
+  static_assert(kLive0 % 16 == 0, "live buffers keep 16-byte alignment");
+  static constexpr int kLiveBars = kLive0 + kWarps * kLive;
+  static constexpr int kBytes = kLiveBars + kWarps * 8;
+};
+
+// WHOLE: every tensor of the launch is aligned for bulk copies and a
+// multiple of 512 elements (the host checked it).
+template <int OPT, int DT, bool WHOLE>
+__global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_constant__ StepArgs a) {
+  using L = SkipSmem<OPT, DT>;
+  constexpr int NS = L::NS;
+  constexpr int NM = L::NM;
+  constexpr int ES = L::ES;
+  constexpr int kStages = L::kStages;
+  extern __shared__ __align__(128) unsigned char ring_smem[];
+  unsigned char* smem = ring_smem;
+  float* sq = reinterpret_cast<float*>(smem + L::kQ);
+  float* smid = reinterpret_cast<float*>(smem + L::kMid);
+  uint32_t* stbl = reinterpret_cast<uint32_t*>(smem + L::kTbl);
+  __shared__ int s_bad[2];
+  __shared__ int s_below[2];
+  __shared__ int s_scan[2 * 32];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned char* ring = smem + L::kRing + warp * kStages * L::kStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars) + warp * kStages;
+  unsigned char* live = smem + L::kLive0 + warp * L::kLive;
+  uint64_t* lbar = reinterpret_cast<uint64_t*>(smem + L::kLiveBars) + warp;
+
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  const int32_t NG = static_cast<int32_t>(gridDim.x) * nwarps;
+  const int32_t b0 = static_cast<int32_t>(blockIdx.x) * nwarps + warp;
+  const int32_t TB = static_cast<int32_t>(a.ring_units);
+
+  // ---- the ring of gradient chunks, and the live buffer ----
+  if (lane < kStages) mbar_init(bars + lane, 1);   // the bulk copy's arrival
+  if (lane == 0) mbar_init(lbar, 2);               // the bulk copies' arrival and the absmax copies'
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+  auto issue = [&](const ChunkRef& c, int s) {
+    const DevTensor& d = a.t[c.t];
+    mbar_expect_tx(bars + s, kChunk * ES);
+    bulk_g2s(ring + s * L::kStage + L::kSG, static_cast<const unsigned char*>(d.g) + c.e0 * ES,
+             kChunk * ES, bars + s);
+  };
+  uint32_t phase = 0u, want = 0u, inflight = 0u;
+  uint32_t lphase = 0u;
+  bool linflight = false;
+  ChunkCursor cur{0, b0};
+  cursor_settle(a, cur);
+  auto put_header = [&](const ChunkRef& c, int s) {
+    if (lane == 0)
+      *reinterpret_cast<int4*>(ring + s * L::kStage + L::kSH) =
+          make_int4(static_cast<int>(c.e0), static_cast<int>(c.e0 >> 32), c.u, c.t | (c.v << 16));
+  };
+  for (int s = 0; s < kStages; ++s) {
+    if (b0 + s * NG < TB) {
+      const ChunkRef c = cursor_chunk<WHOLE>(a, cur, 0);
+      put_header(c, s);
+      if (WHOLE || (c.v == kChunk && (a.t[c.t].vec_ok & 2))) {
+        if (lane == 0) issue(c, s);
+        want |= 1u << s;
+        inflight |= 1u << s;
+      }
+      cur.u += NG;
+      cursor_settle(a, cur);
+    }
+  }
+  __syncwarp();
+
+  // ---- maps, midpoints and bucket tables ----
+  for (int i = tid; i < NM * 256; i += blockDim.x) sq[i] = i < 256 ? a.qmap1[i] : a.qmap2[i - 256];
+  if (tid < 2) s_bad[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < NM * 256; i += blockDim.x) {
+    const int m = i >> 8, k = i & 255;
+    smid[i] = k < 255 ? (sq[m * 256 + k] + sq[m * 256 + k + 1]) * 0.5f : 0.0f;
+  }
+  __syncthreads();
+  build_tables<NM>(smid, stbl, s_bad, s_below, s_scan, static_cast<int>(blockDim.x));
+  const bool fast_map[2] = {s_bad[0] == 0, s_bad[1] == 0};
+  const bool nonneg_map[2] = {sq[0] >= 0.0f, NM > 1 && sq[256] >= 0.0f};
+
+  // ---- the chunk loop ----
+  bool ok = true;
+  int s = 0;
+  for (int32_t b = b0; b < TB; b += NG, s = (s + 1 == kStages) ? 0 : s + 1) {
+    ChunkRef c;
+    {
+      const int4 h = *reinterpret_cast<const int4*>(ring + s * L::kStage + L::kSH);
+      c.e0 = static_cast<int64_t>(static_cast<uint32_t>(h.x)) | (static_cast<int64_t>(h.y) << 32);
+      c.u = h.z;
+      c.t = h.w & 0xffff;
+      c.v = h.w >> 16;
+    }
+    const DevTensor& d = a.t[c.t];
+    const bool have = (WHOLE || c.v > 0) && ok;
+    bool staged = false;
+    if ((want >> s) & 1u) {
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, (phase >> s) & 1u, a.wait_ns));
+        if (!ok && lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+      }
+      if (ok) {
+        phase ^= 1u << s;
+        want &= ~(1u << s);
+        inflight &= ~(1u << s);
+        staged = true;
+      }
+    }
+    const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
+    const bool vec = WHOLE || (d.vec_ok & 1) != 0;
+
+    // ---- the gradient of both blocks of the chunk ----
+    float gc[2][8];
+    int vbs[2];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int rest = c.v - 256 * pass;
+      vbs[pass] = WHOLE ? 256 : (rest > 256 ? 256 : (rest > 0 ? rest : 0));
+      if (staged) {
+        stage_load<DT, 2>(ring + s * L::kStage + L::kSG, lane, 2 * pass, gc[pass]);
+      } else if (!WHOLE && have && vbs[pass] > 0) {
+        global_load<DT, 2>(d.g, c.e0, c.v, lane, 2 * pass, gc[pass]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gc[pass][e] = 0.0f;
+      }
+    }
+    // refill this stage with the chunk kStages ahead
+    __syncwarp();
+    if (ok) {
+      const int32_t bn = b + kStages * NG;
+      if (bn < TB) {
+        const ChunkRef cn = cursor_chunk<WHOLE>(a, cur, 0);
+        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        put_header(cn, s);
+        if (WHOLE || (cn.v == kChunk && (a.t[cn.t].vec_ok & 2))) {
+          if (lane == 0) issue(cn, s);
+          want |= 1u << s;
+          inflight |= 1u << s;
+        }
+        cur.u += NG;
+        cursor_settle(a, cur);
+      }
+    }
+    if (!(have && ok)) continue;
+    // a block whose raw gradient is all zero is left as it is
+    bool blk_live[2];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      bool nz = false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nz = nz || gc[pass][e] != 0.0f;   // (absent elements read as 0)
+      blk_live[pass] = __any_sync(0xffffffffu, nz);
+    }
+    if (!blk_live[0] && !blk_live[1]) continue;
+
+    // ---- the live chunk's p, codes and absmax, one round trip ----
+    const bool bulk = WHOLE || (c.v == kChunk && (d.vec_ok & 2));
+    if (bulk) {
+      // (the buffer's previous contents were read before this warp's votes)
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(lbar, kChunk * ES + NS * kChunk);
+        bulk_g2s(live + L::kLP, static_cast<const unsigned char*>(d.p) + c.e0 * ES, kChunk * ES, lbar);
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+          bulk_g2s(live + L::kLC + k * kChunk, code_stream<OPT>(d, k) + c.e0, kChunk, lbar);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          cp_async4(live + L::kLA + 4 * k, absmax_stream<OPT>(d, k) + 2 * c.u);
+          cp_async4(live + L::kLA + 4 * (NS + k), absmax_stream<OPT>(d, k) + 2 * c.u + 1);
+        }
+        cp_async_arrive(lbar);
+      }
+      linflight = true;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(lbar, lphase, a.wait_ns));
+      if (!ok) {
+        if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+        continue;
+      }
+      lphase ^= 1u;
+      linflight = false;
+    }
+
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      if (!blk_live[pass]) continue;
+      const int q0 = 2 * pass;
+      const int vb = vbs[pass];
+      const float (&g)[8] = gc[pass];
+      const int32_t lb = 2 * c.u + pass;
+      float p[8];
+      uint32_t cw[NS][2];
+      float am[NS];
+      if (bulk) {
+        stage_load<DT, 2>(live + L::kLP, lane, q0, p);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) stage_codes<DT, 2>(live + L::kLC + k * kChunk, lane, q0, cw[k]);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) am[k] = reinterpret_cast<const float*>(live + L::kLA)[pass * NS + k];
+      } else {
+        global_load<DT, 2>(d.p, c.e0, c.v, lane, q0, p);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) global_codes<DT, 2>(code_stream<OPT>(d, k), c.e0, c.v, lane, q0, cw[k]);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) am[k] = absmax_stream<OPT>(d, k)[lb];
+      }
+
+      // ---- dequantize and update; a zero raw gradient keeps the element's
+      // ---- parameter and its old (dequantized) states ----
+      constexpr bool kRatio = OPT == ADAM || OPT == ADAMW || OPT == RMSPROP || OPT == ADAGRAD ||
+                              OPT == ADEMAMIX;
+      constexpr int kV = (OPT == ADAM || OPT == ADAMW) ? 1 : (OPT == ADEMAMIX ? 2 : 0);
+      float sv[NS][8];
+      float gk[8];
+      uint32_t mx[NS];
+#pragma unroll
+      for (int k = 0; k < NS; ++k) mx[k] = 0u;
+      uint32_t lo_v = 0xffffffffu, lo_n = 0xffffffffu, nmax = 0u;
+      auto keep = [](bool skip, float old_v, float new_v) { return skip ? old_v : new_v; };
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const bool k0 = g[e] == 0.0f, k1 = g[e + 1] == 0.0f;
+        float2 stt[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          stt[k] = k < NS ? mul2(make_float2(sq[Traits<OPT>::map_of(k) * 256 + code_of<2>(cw[k], e)],
+                                             sq[Traits<OPT>::map_of(k) * 256 + code_of<2>(cw[k], e + 1)]),
+                                 f2(am[k]))
+                          : f2(0.0f);
+        float2 pp = make_float2(p[e], p[e + 1]);
+        float2 gg = mul2(make_float2(g[e], g[e + 1]), f2(a.gscale));
+        if (!Traits<OPT>::DECOUPLED && a.wd != 0.0f) gg = fma2(f2(a.wd), pp, gg);
+        if (OPT == ADAM || OPT == ADAMW) {
+          const float2 m = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
+          const float2 v = fma2(f2(a.b2), stt[1], mul2(f2(a.omb2), mul2(gg, gg)));
+          sv[0][e] = keep(k0, stt[0].x, m.x); sv[0][e + 1] = keep(k1, stt[0].y, m.y);
+          sv[1][e] = keep(k0, stt[1].x, v.x); sv[1][e + 1] = keep(k1, stt[1].y, v.y);
+          lo_n = min_tiny_n(lo_n, make_float2(sv[0][e], sv[0][e + 1]));
+          lo_v = min_tiny_v(lo_v, make_float2(sv[1][e], sv[1][e + 1]));
+        } else if (OPT == RMSPROP || OPT == ADAGRAD) {
+          const float2 v = OPT == RMSPROP ? fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), mul2(gg, gg)))
+                                          : fma2(gg, gg, stt[0]);
+          sv[0][e] = keep(k0, stt[0].x, v.x); sv[0][e + 1] = keep(k1, stt[0].y, v.y);
+          gk[e] = gg.x; gk[e + 1] = gg.y;
+          nmax = absmax_nan(nmax, gg.x, gg.y);
+          lo_n = min_tiny_n(lo_n, gg);
+          lo_v = min_tiny_v(lo_v, make_float2(sv[0][e], sv[0][e + 1]));
+        } else if (OPT == ADEMAMIX) {
+          const float2 m1 = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
+          const float2 m2 = fma2(f2(a.b3t), stt[1], mul2(f2(a.omb3t), gg));
+          const float2 nu = fma2(f2(a.b2), stt[2], mul2(f2(a.omb2), mul2(gg, gg)));
+          sv[0][e] = keep(k0, stt[0].x, m1.x); sv[0][e + 1] = keep(k1, stt[0].y, m1.y);
+          sv[1][e] = keep(k0, stt[1].x, m2.x); sv[1][e + 1] = keep(k1, stt[1].y, m2.y);
+          sv[2][e] = keep(k0, stt[2].x, nu.x); sv[2][e + 1] = keep(k1, stt[2].y, nu.y);
+          const float2 num = fma2(make_float2(sv[0][e], sv[0][e + 1]), f2(a.inv_bc1),
+                                  mul2(f2(a.alpha_t), make_float2(sv[1][e], sv[1][e + 1])));
+          nmax = absmax_nan(nmax, num.x, num.y);
+          lo_n = min_tiny_n(lo_n, num);
+          lo_v = min_tiny_v(lo_v, make_float2(sv[2][e], sv[2][e + 1]));
+        } else if (OPT == MOMENTUM) {
+          const float2 m = fma2(f2(a.b1), stt[0], gg);
+          sv[0][e] = keep(k0, stt[0].x, m.x); sv[0][e + 1] = keep(k1, stt[0].y, m.y);
+          pair_apply<OPT>(a, -eff, pp, m);
+          p[e] = keep(k0, p[e], pp.x); p[e + 1] = keep(k1, p[e + 1], pp.y);
+        } else {  // LION
+          const float2 cc = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
+          float2 u;
+          u.x = cc.x > 0.0f ? 1.0f : (cc.x < 0.0f ? -1.0f : 0.0f);
+          u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
+          const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
+          sv[0][e] = keep(k0, stt[0].x, m.x); sv[0][e + 1] = keep(k1, stt[0].y, m.y);
+          pair_apply<OPT>(a, -eff, pp, u);
+          p[e] = keep(k0, p[e], pp.x); p[e + 1] = keep(k1, p[e + 1], pp.y);
+        }
+      }
+      // absent elements of a partial chunk keep state 0 (they do not count in the absmax)
+      if (!WHOLE && vb < 256) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int o = quad_offset<DT>(lane, q0 + i) - 256 * pass;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (o + e >= vb) {
+#pragma unroll
+              for (int k = 0; k < NS; ++k) sv[k][4 * i + e] = 0.0f;
+              if (OPT == RMSPROP || OPT == ADAGRAD) gk[4 * i + e] = 0.0f;
+            }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) mx[k] = absmax_nan(mx[k], sv[k][e], sv[k][e + 1]);
+      if constexpr (kRatio) {
+        if (OPT == ADAM || OPT == ADAMW) nmax = mx[0];
+        const bool fast = lo_v >= kRatioLoV && lo_n >= kRatioLoN && a.eps_hat >= 0x1p-60f &&
+                          a.eps_hat <= 0x1p20f && mx[kV] <= kRatioMaxV && nmax <= kRatioMaxN;
+        auto numer = [&](int e) -> float2 {
+          if (OPT == RMSPROP || OPT == ADAGRAD) return make_float2(gk[e], gk[e + 1]);
+          if (OPT == ADEMAMIX)
+            return fma2(make_float2(sv[0][e], sv[0][e + 1]), f2(a.inv_bc1),
+                        mul2(f2(a.alpha_t), make_float2(sv[1][e], sv[1][e + 1])));
+          return make_float2(sv[0][e], sv[0][e + 1]);
+        };
+        auto apply = [&](int e, float2 u) {
+          float2 pp = make_float2(p[e], p[e + 1]);
+          pair_apply<OPT>(a, -eff, pp, u);
+          p[e] = keep(g[e] == 0.0f, p[e], pp.x);
+          p[e + 1] = keep(g[e + 1] == 0.0f, p[e + 1], pp.y);
+        };
+        if (fast) {
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            apply(e, ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            apply(e, ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
+        }
+      }
+      ring_store<DT, 2>(d.p, c.e0, WHOLE ? kChunk : c.v, vec, lane, q0, p);
+
+      // ---- the block's new absmax, requantization, codes and absmax ----
+#pragma unroll
+      for (int k = 0; k < NS; ++k) mx[k] = __reduce_max_sync(0xffffffffu, mx[k]);
+      uint32_t enc[NS][8];
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        const int m = Traits<OPT>::map_of(k);
+        const uint32_t* tz = stbl + m * kTblSize + kTblZero;
+        const float inv = rcp_block(__uint_as_float(mx[k]));
+        const bool fastk = fast_map[m] && mx[k] <= 0x7f7fffffu && inv <= FLT_MAX;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (!fastk) enc[k][e] = encode_search(sv[k][e] * inv, smid + m * 256);
+          else if (Traits<OPT>::nonneg(k) && nonneg_map[m]) enc[k][e] = encode_fast_nonneg(sv[k][e], inv, tz);
+          else enc[k][e] = encode_fast(sv[k][e], inv, tz);
+        }
+        uint32_t w[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          w[i] = __byte_perm(__byte_perm(enc[k][4 * i], enc[k][4 * i + 1], 0x0062u),
+                             __byte_perm(enc[k][4 * i + 2], enc[k][4 * i + 3], 0x0062u), 0x5410u);
+        ring_store_codes<DT, 2>(const_cast<uint8_t*>(code_stream<OPT>(d, k)), c.e0, WHOLE ? kChunk : c.v,
+                                vec, lane, q0, w);
+        if (lane == 0) absmax_stream<OPT>(d, k)[lb] = __uint_as_float(mx[k]);
+      }
+    }
+  }
+
+  // ---- a wait ran out: let this warp's copies still in flight land ----
+  if (!ok && lane == 0) {
+    for (int s2 = 0; s2 < kStages; ++s2)
+      if ((inflight >> s2) & 1u) mbar_wait_bounded(bars + s2, (phase >> s2) & 1u, a.wait_ns);
+    if (linflight) mbar_wait_bounded(lbar, lphase, a.wait_ns);
+  }
+}
+
+template <int OPT, int DT, bool WHOLE>
+cudaError_t launch_step8_skip_ring_w(const StepArgs& a, cudaStream_t s) {
+  using L = SkipSmem<OPT, DT>;
+  static std::atomic<unsigned char> configured[kMaxDevices];
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_skip_ring<OPT, DT, WHOLE>),
+                                      L::kBytes, configured);
+  if (e != cudaSuccess) return e;
+  const int threads = L::kWarps * 32;
+  const int64_t need = (a.ring_units + L::kWarps - 1) / L::kWarps;
+  const int grid = static_cast<int>(need < a.nsm ? need : a.nsm);
+  k_step8_skip_ring<OPT, DT, WHOLE><<<grid, threads, L::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+// skip_zeros, blocksize 256 (the caller checks both).
+template <int OPT, int DT>
+cudaError_t launch_step8_skip_ring(const StepArgs& a, cudaStream_t s) {
+  return a.whole ? launch_step8_skip_ring_w<OPT, DT, true>(a, s)
+                 : launch_step8_skip_ring_w<OPT, DT, false>(a, s);
+}
+
+}  // namespace bnb8
