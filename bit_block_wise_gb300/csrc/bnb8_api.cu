@@ -448,12 +448,15 @@ int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int
   return static_cast<int>(need < persistent ? need : persistent);
 }
 
-// max_unorm pre-pass + finalize into out_scale[caller index].
+// max_unorm pre-pass + finalize into out_scale[caller index].  fill: every
+// entry of out_scale is first set to 1 (the caller reads the multipliers of
+// empty tensors too); the step reads only those of the tensors it updates,
+// which the finalize writes, and skips that launch.
 int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparams& hp,
               const Scalars& sc, int log2B, const float* qmap1, const float* qmap2,
-              float* out_scale, float2* partials, cudaStream_t stream,
+              float* out_scale, float2* partials, cudaStream_t stream, bool fill,
               uint64_t* stamp = nullptr, uint64_t carry_expect = 0) {
-  cudaError_t e = launch_fill(out_scale, nt, 1.0f, stream);  // n == 0 tensors keep 1
+  cudaError_t e = fill ? launch_fill(out_scale, nt, 1.0f, stream) : cudaSuccess;  // n == 0 tensors keep 1
   if (e != cudaSuccess) return cuda_fail(e, "unorm fill");
   for (size_t ci = 0; ci < plan.chunks.size(); ++ci) {
     const Plan::Chunk& c = plan.chunks[ci];
@@ -530,7 +533,7 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
     float* scales = reinterpret_cast<float*>(static_cast<char*>(ws) + kStampBytes);
     partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + partials_offset(nt));
     stamp = static_cast<uint64_t*>(ws);
-    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream, stamp,
+    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream, false, stamp,
                    carry ? carry_stamp_for(list, hp->step - 1) : 0);
     if (rc != BNB8_OK) return rc;
     clip = scales;
@@ -783,7 +786,7 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
                 need, workspace_bytes);
   float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) + partials_offset(ntensors));
   const Scalars sc = make_scalars(*hp);
-  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s,
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s, true,
                    static_cast<uint64_t*>(workspace));
 }
 
@@ -859,7 +862,7 @@ extern "C" int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const
   // every partial a call reads is written by the same call's pre-pass first,
   // so the contents left by an earlier call need no clearing
   const Scalars sc = make_scalars(*hp);
-  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s);
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s, true);
 }
 
 // ---------------------------------------------------------------------------

@@ -470,6 +470,8 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
   // the pre-pass with a carried parameter norm
   const bool carried = NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
   const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));
+  // the pre-pass's directions from the hardware approximations
+  const bool approx = NORM && ratio_approx_ok(a.eps_hat);
 
   // ---- the ring: barriers, then the first chunks' copies ----
   if (lane < kStages) mbar_init(bars + lane, 2);   // the bulk copies' arrival and the absmax copies'
@@ -780,16 +782,20 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
             const float2 v = fma2(f2(a.b2), stt[1], mul2(f2(a.omb2), mul2(gg, gg)));
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
             sv[1][e] = v.x; sv[1][e + 1] = v.y;
-            lo_n = min_tiny_n(lo_n, m);
-            lo_v = min_tiny_v(lo_v, v);
+            if (!NORM) {
+              lo_n = min_tiny_n(lo_n, m);
+              lo_v = min_tiny_v(lo_v, v);
+            }
           } else if (OPT == RMSPROP || OPT == ADAGRAD) {
             const float2 v = OPT == RMSPROP ? fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), mul2(gg, gg)))
                                             : fma2(gg, gg, stt[0]);
             sv[0][e] = v.x; sv[0][e + 1] = v.y;
             gk[e] = gg.x; gk[e + 1] = gg.y;
-            nmax = absmax_nan(nmax, gg.x, gg.y);
-            lo_n = min_tiny_n(lo_n, gg);
-            lo_v = min_tiny_v(lo_v, v);
+            if (!NORM) {
+              nmax = absmax_nan(nmax, gg.x, gg.y);
+              lo_n = min_tiny_n(lo_n, gg);
+              lo_v = min_tiny_v(lo_v, v);
+            }
           } else if (OPT == ADEMAMIX) {
             const float2 m1 = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
             const float2 m2 = fma2(f2(a.b3t), stt[1], mul2(f2(a.omb3t), gg));
@@ -798,9 +804,11 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
             sv[0][e] = m1.x; sv[0][e + 1] = m1.y;
             sv[1][e] = m2.x; sv[1][e + 1] = m2.y;
             sv[2][e] = nu.x; sv[2][e + 1] = nu.y;
-            nmax = absmax_nan(nmax, num.x, num.y);
-            lo_n = min_tiny_n(lo_n, num);
-            lo_v = min_tiny_v(lo_v, nu);
+            if (!NORM) {
+              nmax = absmax_nan(nmax, num.x, num.y);
+              lo_n = min_tiny_n(lo_n, num);
+              lo_v = min_tiny_v(lo_v, nu);
+            }
           } else if (OPT == MOMENTUM) {
             const float2 m = fma2(f2(a.b1), stt[0], gg);
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
@@ -841,12 +849,35 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
               }
           }
         }
+        // (the pre-pass requantizes nothing: no absmax)
+        if constexpr (!NORM) {
 #pragma unroll
-        for (int k = 0; k < NS; ++k)
+          for (int k = 0; k < NS; ++k)
 #pragma unroll
-          for (int e = 0; e < NE; e += 2)
-            mx[half_of(e)][k] = absmax_nan(mx[half_of(e)][k], sv[k][e], sv[k][e + 1]);
-        if constexpr (kRatio) {
+            for (int e = 0; e < NE; e += 2)
+              mx[half_of(e)][k] = absmax_nan(mx[half_of(e)][k], sv[k][e], sv[k][e + 1]);
+        }
+        if constexpr (kRatio && NORM) {
+          // the pre-pass: u only for its norm, from the hardware
+          // approximations (within 2^-21 relative) where eps allows, else
+          // from the IEEE operations
+          auto numer = [&](int e) -> float2 {
+            if (OPT == RMSPROP || OPT == ADAGRAD) return make_float2(gk[e], gk[e + 1]);
+            if (OPT == ADEMAMIX)
+              return fma2(make_float2(sv[0][e], sv[0][e + 1]), f2(a.inv_bc1),
+                          mul2(f2(a.alpha_t), make_float2(sv[1][e], sv[1][e + 1])));
+            return make_float2(sv[0][e], sv[0][e + 1]);
+          };
+          if (approx) {
+#pragma unroll
+            for (int e = 0; e < NE; e += 2)
+              add_u2(e, ratio2_approx(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
+          } else {
+#pragma unroll
+            for (int e = 0; e < NE; e += 2)
+              add_u2(e, ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
+          }
+        } else if constexpr (kRatio) {
           // pass 2: u = n / (sqrt(v) + eps) and the new p; the fast ratio
           // when every operand of the lane lies in its range, the IEEE
           // operations else
