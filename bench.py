@@ -525,8 +525,8 @@ def run_gpu(args, wl):
     n_chunks32 = -(-sum(1 for b in wl.bits if b == 32) // 96)
     launches_per_step = n_chunks8 + n_chunks32
     if wl.hp.get("max_unorm", 0.0) > 0 and not wl.hp.get("unorm_per_block"):
-        # fill + per chunk: pre-pass, chunk sums, finalize
-        launches_per_step += 1 + 3 * (n_chunks8 + n_chunks32)
+        # per launch group: pre-pass, reduction (chunk sums and multipliers)
+        launches_per_step += 2 * (n_chunks8 + n_chunks32)
     if wl.blocksize == 0:
         launches_per_step += 1 + 2 * n_chunks8                  # fill + absmax pass + store
 

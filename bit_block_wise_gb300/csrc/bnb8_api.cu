@@ -8,6 +8,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -300,14 +301,17 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // Workspace layout when the per-tensor pre-pass runs: [the carried norm's
 // stamp, in its own 256 bytes][per-tensor max_unorm multipliers][per-block
-// partials]; then [4 words per tensor] of tensor-wise absmax accumulators
-// when blocksize is 0.  The stamp sits at the same place for every tensor
-// list, so any call that reuses the workspace for another list replaces it.
+// partials][the reduction's tickets, one word per tensor of a launch]; then
+// [4 words per tensor] of tensor-wise absmax accumulators when blocksize is
+// 0.  The stamp sits at the same place for every tensor list, so any call
+// that reuses the workspace for another list replaces it.
 constexpr size_t kStampBytes = 256;
+constexpr size_t kTicketBytes = (kMaxTensors * sizeof(uint32_t) + 255) / 256 * 256;
 size_t partials_offset(int nt) { return kStampBytes + align256(static_cast<size_t>(nt) * sizeof(float)); }
-size_t workspace_bytes_for(int nt, int64_t all_blocks) {
+size_t tickets_offset(int nt, int64_t all_blocks) {
   return partials_offset(nt) + align256(static_cast<size_t>(all_blocks) * sizeof(float2));
 }
+size_t workspace_bytes_for(int nt, int64_t all_blocks) { return tickets_offset(nt, all_blocks) + kTicketBytes; }
 
 // The carried norm's stamp: a hash of the tensor list and the settings that
 // shape its partials (FNV-1a over 64-bit words), mixed with a step number.
@@ -454,7 +458,7 @@ int grid_for(int bits, int optim, int dtype, int mode, int64_t total_blocks, int
 // which the finalize writes, and skips that launch.
 int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparams& hp,
               const Scalars& sc, int log2B, const float* qmap1, const float* qmap2,
-              float* out_scale, float2* partials, cudaStream_t stream, bool fill,
+              float* out_scale, float2* partials, uint32_t* tickets, cudaStream_t stream, bool fill,
               uint64_t* stamp = nullptr, uint64_t carry_expect = 0) {
   cudaError_t e = fill ? launch_fill(out_scale, nt, 1.0f, stream) : cudaSuccess;  // n == 0 tensors keep 1
   if (e != cudaSuccess) return cuda_fail(e, "unorm fill");
@@ -465,6 +469,7 @@ int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparam
     // carry_expect 0: no carried norm (a stamp is never 0)
     a.carry_stamp = carry_expect != 0 ? stamp : nullptr;
     a.carry_expect = carry_expect;
+    a.tickets = tickets;   // zeroed by the pre-pass for the reduction that follows
     const int grid = grid_for(c.bits, hp.optim, hp.dtype, MODE_NORM, c.total_blocks, log2B);
     e = launch_family(c.bits, hp.optim, hp.dtype, MODE_NORM, a, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "unorm pre-pass launch");
@@ -475,6 +480,7 @@ int run_unorm(const Plan& plan, const bnb8_tensor* ts, int nt, const bnb8_hparam
     f.unorm_c = sc.unorm_c;
     f.max_unorm = hp.max_unorm;
     f.ntensors = a.ntensors;
+    f.tickets = tickets;
     // these partials no longer hold a carried norm: the last finalize clears
     // the stamp (a step that carries the norm writes a new one after it)
     f.stamp_clear = ci + 1 == plan.chunks.size() ? stamp : nullptr;
@@ -533,7 +539,8 @@ int step_common(const bnb8_tensor* ts, int nt, const bnb8_hparams* hp, const int
     float* scales = reinterpret_cast<float*>(static_cast<char*>(ws) + kStampBytes);
     partials = reinterpret_cast<float2*>(static_cast<char*>(ws) + partials_offset(nt));
     stamp = static_cast<uint64_t*>(ws);
-    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, stream, false, stamp,
+    uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + tickets_offset(nt, plan.all_blocks));
+    rc = run_unorm(plan, ts, nt, *hp, sc, log2B, qmap1, qmap2, scales, partials, tickets, stream, false, stamp,
                    carry ? carry_stamp_for(list, hp->step - 1) : 0);
     if (rc != BNB8_OK) return rc;
     clip = scales;
@@ -785,8 +792,10 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
     return fail(BNB8_EWORKSPACE, "unorm needs a 256-byte aligned workspace of %zu bytes (got %zu)",
                 need, workspace_bytes);
   float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) + partials_offset(ntensors));
+  uint32_t* tickets =
+      reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + tickets_offset(ntensors, plan.all_blocks));
   const Scalars sc = make_scalars(*hp);
-  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s, true,
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, tickets, s, true,
                    static_cast<uint64_t*>(workspace));
 }
 
@@ -802,26 +811,30 @@ namespace {
 
 constexpr int64_t kStaticScratchBlocks = int64_t(1) << 18;  // float2 partials: 2 MiB
 
-__device__ __align__(256) float2 g_static_scratch[kStaticScratchBlocks];
+struct StaticScratch {
+  float2 partials[kStaticScratchBlocks];
+  uint32_t tickets[kMaxTensors];
+};
+__device__ __align__(256) StaticScratch g_static_scratch;
 
 // Device address of g_static_scratch on the current device, looked up once per
 // device (with that device current) and cached.  Host code must not use the
 // array's name as a pointer: on the host it only stands in for the symbol.
 // The cache entries are atomics: host threads making their first call on a
 // device at the same time both look the address up and store the same value.
-int static_scratch(float2** out) {
-  static std::atomic<float2*> addr[kMaxDevices];
+int static_scratch(StaticScratch** out) {
+  static std::atomic<StaticScratch*> addr[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return fail(BNB8_EUNSUPPORTED, "device ordinal %d out of range", dev);
-  float2* a = addr[dev].load(std::memory_order_acquire);
+  StaticScratch* a = addr[dev].load(std::memory_order_acquire);
   if (a == nullptr) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    a = static_cast<float2*>(ptr);
+    a = static_cast<StaticScratch*>(ptr);
     addr[dev].store(a, std::memory_order_release);
   }
   *out = a;
@@ -856,13 +869,17 @@ extern "C" int bnb8_unorm_static(const bnb8_tensor* tensors, int ntensors, const
     const cudaError_t e = launch_fill(out_scale, ntensors, 1.0f, s);
     return e == cudaSuccess ? BNB8_OK : cuda_fail(e, "unorm fill");
   }
-  float2* partials = nullptr;
-  rc = static_scratch(&partials);
+  StaticScratch* scratch = nullptr;
+  rc = static_scratch(&scratch);
   if (rc != BNB8_OK) return rc;
   // every partial a call reads is written by the same call's pre-pass first,
-  // so the contents left by an earlier call need no clearing
+  // and the pre-pass zeroes the tickets, so the contents left by an earlier
+  // call need no clearing
   const Scalars sc = make_scalars(*hp);
-  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale, partials, s, true);
+  char* base = reinterpret_cast<char*>(scratch);   // a device address: offsets only
+  return run_unorm(plan, tensors, ntensors, *hp, sc, log2B, qmap1, qmap2, out_scale,
+                   reinterpret_cast<float2*>(base + offsetof(StaticScratch, partials)),
+                   reinterpret_cast<uint32_t*>(base + offsetof(StaticScratch, tickets)), s, true);
 }
 
 // ---------------------------------------------------------------------------

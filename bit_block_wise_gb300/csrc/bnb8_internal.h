@@ -104,6 +104,9 @@ struct StepArgs {
   uint64_t* carry_stamp;
   uint64_t carry_expect;
   uint64_t carry_write;
+  // MODE_NORM: the per-tensor tickets of the reduction that follows (CTA 0
+  // sets tickets[0, ntensors) to 0), or null
+  uint32_t* tickets;
   DevTensor t[kMaxTensors];
 };
 
@@ -126,11 +129,13 @@ struct DequantArgs {
   int32_t log2B;
 };
 
-// The per-tensor max_unorm reduction of the pre-pass's block partials, in two
-// levels: k_unorm_chunks sums each chunk of kUnormChunk blocks of a tensor in
-// binary64 (one CTA per chunk) and writes the two sums in place over the
-// chunk's first two partials; k_unorm_finalize adds a tensor's chunk sums (a
-// one-block chunk keeps its binary32 partial) and writes the multiplier.
+// The per-tensor max_unorm reduction of the pre-pass's block partials, one
+// launch in two levels: a CTA per chunk of kUnormChunk blocks of a tensor sums
+// the chunk in binary64 and writes the two sums in place over the chunk's
+// first two partials; the CTA that completes a tensor's last chunk (a ticket
+// per tensor, zeroed by the pre-pass) adds the tensor's chunk sums in chunk
+// order (a one-block chunk keeps its binary32 partial) and writes the
+// multiplier.
 constexpr int64_t kUnormChunk = 512;
 
 struct FinalizeArgs {
@@ -143,6 +148,7 @@ struct FinalizeArgs {
   int64_t first_chunk[kMaxTensors + 1];  // chunks of tensors 0..t-1
   int32_t index[kMaxTensors];
   uint64_t* stamp_clear;   // set to 0 (the carried norm's stamp), or null
+  uint32_t* tickets;       // [ntensors], zero on entry
 };
 
 // Kernel launchers (defined in the kernel translation units).  Each returns
@@ -174,7 +180,7 @@ BNB8_DECLARE_OPT(ADEMAMIX)
 #undef BNB8_DECLARE_OPT
 cudaError_t launch_quantize(int dtype, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);  // both levels
+cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s);  // both levels, one launch
 cudaError_t launch_fill(float* out, int n, float v, cudaStream_t s);
 
 // Resident CTAs per SM of a step kernel (sizes the persistent grids).

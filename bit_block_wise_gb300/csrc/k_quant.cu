@@ -102,71 +102,77 @@ __global__ void __launch_bounds__(256) k_dequantize(const __grid_constant__ Dequ
   }
 }
 
-// Level 1: one CTA per chunk of up to kUnormChunk blocks of one tensor.  Its
+// One CTA per chunk of up to kUnormChunk blocks of one tensor.  Level 1: its
 // binary64 sums (sum u^2, sum p^2) in a fixed order (thread i takes blocks i,
-// i + 256, ...; then a tree) replace the chunk's first two partials.  Chunks
-// of a single block are left as they are.
-__global__ void __launch_bounds__(256) k_unorm_chunks(const __grid_constant__ FinalizeArgs a) {
+// i + 256, ...; then a tree) replace the chunk's first two partials (a chunk
+// of a single block is left as it is).  Level 2, in the CTA that takes the
+// tensor's last ticket: the tensor's chunk sums in the same fixed order
+// (thread i takes chunks i, i + 256, ...; then a tree), and the multiplier.
+__global__ void __launch_bounds__(256) k_unorm_reduce(const __grid_constant__ FinalizeArgs a) {
   __shared__ double su[256], sp[256];
+  __shared__ int s_last;
   const int64_t c = blockIdx.x;
-  int t = 0;
-  while (t + 1 < a.ntensors && a.first_chunk[t + 1] <= c) ++t;
+  // the tensor of chunk c: the last t with first_chunk[t] <= c
+  int lo = 0, hi = a.ntensors - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.first_chunk[mid] <= c) lo = mid;
+    else hi = mid - 1;
+  }
+  const int t = lo;
+  auto tree = [&](double u, double p) {
+    su[threadIdx.x] = u;
+    sp[threadIdx.x] = p;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+      if (threadIdx.x < o) {
+        su[threadIdx.x] += su[threadIdx.x + o];
+        sp[threadIdx.x] += sp[threadIdx.x + o];
+      }
+      __syncthreads();
+    }
+  };
   const int64_t b0 = a.first_block[t] + (c - a.first_chunk[t]) * kUnormChunk;
   const int64_t b1 = b0 + kUnormChunk < a.first_block[t + 1] ? b0 + kUnormChunk : a.first_block[t + 1];
-  if (b1 - b0 < 2) return;
-  double u = 0.0, p = 0.0;
-  for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
-    const float2 v = a.partials[b];
-    u += static_cast<double>(v.x);
-    p += static_cast<double>(v.y);
-  }
-  su[threadIdx.x] = u;
-  sp[threadIdx.x] = p;
-  __syncthreads();  // every partial of the chunk has been read
-  for (int o = 128; o > 0; o >>= 1) {
-    if (threadIdx.x < o) {
-      su[threadIdx.x] += su[threadIdx.x + o];
-      sp[threadIdx.x] += sp[threadIdx.x + o];
+  if (b1 - b0 >= 2) {
+    double u = 0.0, p = 0.0;
+    for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) {
+      const float2 v = a.partials[b];
+      u += static_cast<double>(v.x);
+      p += static_cast<double>(v.y);
     }
-    __syncthreads();
+    tree(u, p);   // (every partial of the chunk has been read before the first barrier)
+    if (threadIdx.x == 0) {
+      double* out = reinterpret_cast<double*>(a.partials + b0);
+      out[0] = su[0];
+      out[1] = sp[0];
+    }
   }
-  if (threadIdx.x == 0) {
-    double* out = reinterpret_cast<double*>(a.partials + b0);
-    out[0] = su[0];
-    out[1] = sp[0];
-  }
-}
-
-// Level 2: one CTA per tensor adds the tensor's chunk sums in chunk order and
-// writes the step multiplier.
-__global__ void __launch_bounds__(256) k_unorm_finalize(const __grid_constant__ FinalizeArgs a) {
-  __shared__ double su[256], sp[256];
-  const int t = blockIdx.x;
+  // the ticket: the sums above are visible device-wide before it is taken
   const int64_t nchunks = a.first_chunk[t + 1] - a.first_chunk[t];
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.tickets + t, 1u) + 1u == static_cast<uint32_t>(nchunks);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
   double u = 0.0, p = 0.0;
-  for (int64_t c = threadIdx.x; c < nchunks; c += blockDim.x) {
-    const int64_t b0 = a.first_block[t] + c * kUnormChunk;
-    const int64_t b1 = b0 + kUnormChunk < a.first_block[t + 1] ? b0 + kUnormChunk : a.first_block[t + 1];
-    if (b1 - b0 >= 2) {
-      const double* in = reinterpret_cast<const double*>(a.partials + b0);
-      u += in[0];
-      p += in[1];
+  for (int64_t k = threadIdx.x; k < nchunks; k += blockDim.x) {
+    const int64_t k0 = a.first_block[t] + k * kUnormChunk;
+    const int64_t k1 = k0 + kUnormChunk < a.first_block[t + 1] ? k0 + kUnormChunk : a.first_block[t + 1];
+    if (k1 - k0 >= 2) {
+      // written by other CTAs: read past the L1
+      const double* in = reinterpret_cast<const double*>(a.partials + k0);
+      u += __ldcg(in);
+      p += __ldcg(in + 1);
     } else {
-      const float2 v = a.partials[b0];
+      const float2 v = __ldcg(a.partials + k0);
       u += static_cast<double>(v.x);
       p += static_cast<double>(v.y);
     }
   }
-  su[threadIdx.x] = u;
-  sp[threadIdx.x] = p;
-  __syncthreads();
-  for (int o = 128; o > 0; o >>= 1) {
-    if (threadIdx.x < o) {
-      su[threadIdx.x] += su[threadIdx.x + o];
-      sp[threadIdx.x] += sp[threadIdx.x + o];
-    }
-    __syncthreads();
-  }
+  tree(u, p);
   if (threadIdx.x == 0) {
     const double unorm = a.unorm_c * sqrt(su[0]);
     const double limit = a.max_unorm * sqrt(sp[0]);
@@ -214,13 +220,9 @@ cudaError_t launch_dequantize(int dtype, const DequantArgs& a, int grid, cudaStr
 }
 
 cudaError_t launch_unorm_finalize(const FinalizeArgs& a, cudaStream_t s) {
-  const int64_t chunks = a.first_chunk[a.ntensors];
-  if (chunks > 0) {
-    k_unorm_chunks<<<static_cast<unsigned>(chunks), 256, 0, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  k_unorm_finalize<<<a.ntensors, 256, 0, s>>>(a);
+  const int64_t chunks = a.first_chunk[a.ntensors];   // >= 1 per tensor (no empty tensor)
+  if (chunks <= 0) return cudaSuccess;
+  k_unorm_reduce<<<static_cast<unsigned>(chunks), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

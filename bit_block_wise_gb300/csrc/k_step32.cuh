@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step32(const __grid_constant__ 
   const int64_t warp_g0 = static_cast<int64_t>(blockIdx.x) * groups_per_cta + ((tid & ~31) / GT);
   const int in_warp = GT < 32 ? lane / GT : 0;
   int parity = 0;
+  // the pre-pass zeroes the tickets of the reduction launched after it
+  if (MODE == MODE_NORM && a.tickets != nullptr && blockIdx.x == 0 && tid < a.ntensors) a.tickets[tid] = 0u;
   // the pre-pass with a carried parameter norm (see k_step8)
   const bool carried = MODE == MODE_NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
   const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));

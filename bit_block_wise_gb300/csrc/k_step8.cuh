@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_step8(const __grid_constant__ S
   __shared__ int s_scan[2 * 32];
 
   const int tid = threadIdx.x;
+  // the pre-pass zeroes the tickets of the reduction launched after it
+  if (MODE == MODE_NORM && a.tickets != nullptr && blockIdx.x == 0 && tid < a.ntensors) a.tickets[tid] = 0u;
   // the pre-pass with a carried parameter norm (BNB8_CARRY_PNORM): the sums
   // of p^2 are already in the partials; p is not read when the direction does
   // not depend on it

@@ -467,6 +467,8 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
   const int32_t NG = static_cast<int32_t>(gridDim.x) * gpc;
   const int32_t b0 = static_cast<int32_t>(blockIdx.x) * gpc + warp / G;
   const int32_t TB = static_cast<int32_t>(a.ring_units);
+  // the pre-pass zeroes the tickets of the reduction launched after it
+  if (NORM && a.tickets != nullptr && blockIdx.x == 0 && tid < a.ntensors) a.tickets[tid] = 0u;
   // the pre-pass with a carried parameter norm
   const bool carried = NORM && a.carry_stamp != nullptr && *a.carry_stamp == a.carry_expect;
   const bool read_p = !(carried && (Traits<OPT>::DECOUPLED || a.wd == 0.0f));

@@ -240,8 +240,9 @@ int bnb8_dequantize_blockwise(const uint8_t* codes, const float* absmax, const f
                               struct CUstream_st* stream);
 
 /* Bytes of workspace the step functions and bnb8_unorm need for this tensor
- * list: the per-tensor max_unorm pre-pass's stamp, multipliers and partials
- * (hp->max_unorm > 0 without BNB8_UNORM_PER_BLOCK) plus 16 bytes per tensor for tensor-wise
+ * list: the per-tensor max_unorm pre-pass's stamp, multipliers, partials and
+ * the reduction's tickets (hp->max_unorm > 0 without BNB8_UNORM_PER_BLOCK)
+ * plus 16 bytes per tensor for tensor-wise
  * quantization (hp->blocksize 0); 0 when neither applies.  Returns 0 and
  * sets the error message on invalid arguments. */
 size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp);
@@ -308,10 +309,11 @@ int bnb8_unorm(const bnb8_tensor* tensors, int ntensors, const bnb8_hparams* hp,
  * memory: for example code whose device memory is all handed out by a host
  * framework's pool that must see every allocation, or a hot loop where a
  * cudaMalloc / cudaFree would stall the device.  This entry point calls no
- * allocator; its scratch (the per-block partial norms) is a fixed array of
- * 262,144 blocks (2 MiB) compiled into the library, which every GPU that
- * loads the library holds until the process exits.  The paper has no
- * counterpart: this is a deployment variant of bnb8_unorm.
+ * allocator; its scratch (the per-block partial norms of up to 262,144
+ * blocks, 2 MiB, and the reduction's tickets) is a fixed array compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  The paper has no counterpart: this is a deployment variant of
+ * bnb8_unorm.
  *   Same arguments, results and errors as bnb8_unorm, minus the workspace.
  *   A list with more than 262,144 blocks (over all tensors, at hp->blocksize)
  *   is rejected with BNB8_EWORKSPACE.

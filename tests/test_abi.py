@@ -172,8 +172,9 @@ def test_workspace_size_and_check(L):
     hp = _hp(max_unorm=1.0)
     need = L.bnb8_workspace_size(arr, 4, ctypes.byref(hp))
     blocks = 4 + 3 + 0 + 1
-    # the carried norm's stamp, the multipliers, one float2 partial per block
-    assert need == 256 + 256 + ((blocks * 8 + 255) // 256) * 256
+    # the carried norm's stamp, the multipliers, one float2 partial per block,
+    # the reduction's tickets (one word for each of up to 96 tensors a launch)
+    assert need == 256 + 256 + ((blocks * 8 + 255) // 256) * 256 + 512
     assert _call2(L, ts, hp, ws=None, wsb=0) == bnb8.BNB8_EWORKSPACE
     assert _call2(L, ts, hp, ws=FAKE, wsb=need - 1) == bnb8.BNB8_EWORKSPACE
     assert _call2(L, ts, hp, ws=FAKE + 8, wsb=need) == bnb8.BNB8_EWORKSPACE
