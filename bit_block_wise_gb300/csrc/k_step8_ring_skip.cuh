@@ -77,18 +77,30 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
   __shared__ int s_bad[2];
   __shared__ int s_below[2];
   __shared__ int s_scan[2 * 32];
+  __shared__ int32_t s_next;   // the CTA's next chunk to hand out
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_next = 0;
+  __syncthreads();
   unsigned char* ring = smem + L::kRing + warp * kStages * L::kStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars) + warp * kStages;
   unsigned char* live = smem + L::kLive0 + warp * L::kLive;
   uint64_t* lbar = reinterpret_cast<uint64_t*>(smem + L::kLiveBars) + warp;
 
-  const int nwarps = static_cast<int>(blockDim.x >> 5);
-  const int32_t NG = static_cast<int32_t>(gridDim.x) * nwarps;
-  const int32_t b0 = static_cast<int32_t>(blockIdx.x) * nwarps + warp;
+  // The CTA's units are blockIdx.x + k * gridDim.x; its warps take the next
+  // k from a shared counter as they go (a warp's units still ascend).  Live
+  // chunks cost far more than dead ones and fall at random, so a fixed
+  // share per warp would leave the warp with the most live chunks running
+  // long after the others.
   const int32_t TB = static_cast<int32_t>(a.ring_units);
+  auto grab = [&]() -> int32_t {
+    int32_t k = 0;
+    if (lane == 0) k = atomicAdd(&s_next, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    const int64_t u = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
+    return u < TB ? static_cast<int32_t>(u) : TB;
+  };
 
   // ---- the ring of gradient chunks, and the live buffer ----
   if (lane < kStages) mbar_init(bars + lane, 1);   // the bulk copy's arrival
@@ -104,25 +116,31 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
   uint32_t phase = 0u, want = 0u, inflight = 0u;
   uint32_t lphase = 0u;
   bool linflight = false;
-  ChunkCursor cur{0, b0};
-  cursor_settle(a, cur);
+  ChunkCursor cur{0, 0};
+  int32_t at = 0;              // the cursor's unit over the launch
+  uint32_t held = 0u;          // stages holding a chunk
+  auto move_to = [&](int32_t un) {
+    cur.u += un - at;
+    at = un;
+    cursor_settle(a, cur);
+  };
   auto put_header = [&](const ChunkRef& c, int s) {
     if (lane == 0)
       *reinterpret_cast<int4*>(ring + s * L::kStage + L::kSH) =
           make_int4(static_cast<int>(c.e0), static_cast<int>(c.e0 >> 32), c.u, c.t | (c.v << 16));
   };
   for (int s = 0; s < kStages; ++s) {
-    if (b0 + s * NG < TB) {
-      const ChunkRef c = cursor_chunk<WHOLE>(a, cur, 0);
-      put_header(c, s);
-      if (WHOLE || (c.v == kChunk && (a.t[c.t].vec_ok & 2))) {
-        if (lane == 0) issue(c, s);
-        want |= 1u << s;
-        inflight |= 1u << s;
-      }
-      cur.u += NG;
-      cursor_settle(a, cur);
+    const int32_t un = grab();
+    if (un >= TB) break;
+    move_to(un);
+    const ChunkRef c = cursor_chunk<WHOLE>(a, cur, 0);
+    put_header(c, s);
+    if (WHOLE || (c.v == kChunk && (a.t[c.t].vec_ok & 2))) {
+      if (lane == 0) issue(c, s);
+      want |= 1u << s;
+      inflight |= 1u << s;
     }
+    held |= 1u << s;
   }
   __syncwarp();
 
@@ -141,8 +159,9 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
 
   // ---- the chunk loop ----
   bool ok = true;
-  int s = 0;
-  for (int32_t b = b0; b < TB; b += NG, s = (s + 1 == kStages) ? 0 : s + 1) {
+  // the stages are refilled in turn, so those holding a chunk follow each
+  // other from s on; the loop ends at the first empty one
+  for (int s = 0; (held >> s) & 1u; s = (s + 1 == kStages) ? 0 : s + 1) {
     ChunkRef c;
     {
       const int4 h = *reinterpret_cast<const int4*>(ring + s * L::kStage + L::kSH);
@@ -185,11 +204,13 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
         for (int e = 0; e < 8; ++e) gc[pass][e] = 0.0f;
       }
     }
-    // refill this stage with the chunk kStages ahead
+    // refill this stage with the warp's next chunk
     __syncwarp();
+    held &= ~(1u << s);
     if (ok) {
-      const int32_t bn = b + kStages * NG;
-      if (bn < TB) {
+      const int32_t un = grab();
+      if (un < TB) {
+        move_to(un);
         const ChunkRef cn = cursor_chunk<WHOLE>(a, cur, 0);
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         put_header(cn, s);
@@ -198,8 +219,7 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
           want |= 1u << s;
           inflight |= 1u << s;
         }
-        cur.u += NG;
-        cursor_settle(a, cur);
+        held |= 1u << s;
       }
     }
     if (!(have && ok)) continue;
