@@ -109,6 +109,13 @@ struct RingShape {
   static constexpr int kNE = 4 * kQuads;                 // elements a lane per pass
 };
 enum RingShapeId { SH_ONE = 0, SH_TWO = 1, SH_BIG = 2 };
+// Warps per CTA: the two-pass shapes run 24 warps of at most 80 registers,
+// AdEMAMix (three states) 20 warps of at most 96; the one-pass shape 16 of
+// at most 128.
+template <int OPT, int SH>
+__host__ __device__ constexpr int ring_warps() {
+  return SH == SH_ONE ? 16 : (OPT == ADEMAMIX ? 20 : 24);
+}
 template <int OPT, int DT, int SH>
 struct RingSmem {
   static constexpr bool SEQ = SH != SH_ONE;
@@ -134,7 +141,7 @@ struct RingSmem {
   // the opt-in shared memory of an sm_100-class CTA (227 KB), less room for
   // the kernel's static shared variables
   static constexpr int kBudget = 232448 - 1024;
-  static constexpr int kWarps = RingShape<SEQ>::kWarps;
+  static constexpr int kWarps = ring_warps<OPT, SH>();
   // two stages where they fit (while one chunk is computed the next is in
   // flight), else one: a chunk is read into registers first thing, so the
   // copy of the next one overlaps the rest of the iteration
@@ -428,7 +435,7 @@ __device__ __forceinline__ float2 ring_group_sum2(float2 v, int G, int warp, int
 // step.
 enum RingMode { RING_STEP = 0, RING_NORM = 1, RING_BCLIP = 2 };
 template <int OPT, int DT, bool WHOLE, int SH, int RM>
-__global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
+__global__ void __launch_bounds__(ring_warps<OPT, SH>() * 32, 1)
     k_step8_ring(const __grid_constant__ StepArgs a) {
   constexpr bool NORM = RM == RING_NORM;
   constexpr bool BCLIP = RM == RING_BCLIP;
@@ -1175,11 +1182,10 @@ __global__ void __launch_bounds__(RingShape<SH != SH_ONE>::kWarps * 32, 1)
 
 // CTA size for a launch: as many warps as the ring holds, whole groups.
 // (at most 15 groups: named barriers 1..15 are the groups' meeting points)
-template <int SH>
+template <int OPT, int SH>
 __host__ __forceinline__ int ring_threads(int log2B) {
-  constexpr bool SEQ = SH != SH_ONE;
   const int G = log2B > kLog2Chunk ? (1 << (log2B - kLog2Chunk)) : 1;
-  int groups = RingShape<SEQ>::kWarps / G;
+  int groups = ring_warps<OPT, SH>() / G;
   if (G > 1 && groups > 15) groups = 15;
   return groups * G * 32;
 }
@@ -1191,7 +1197,7 @@ cudaError_t launch_step8_ring_w(const StepArgs& a, cudaStream_t s) {
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k_step8_ring<OPT, DT, WHOLE, SH, RM>),
                                       L::kBytes, configured);
   if (e != cudaSuccess) return e;
-  const int threads = ring_threads<SH>(a.log2B);
+  const int threads = ring_threads<OPT, SH>(a.log2B);
   const int G = a.log2B > kLog2Chunk ? (1 << (a.log2B - kLog2Chunk)) : 1;
   const int64_t groups = threads / 32 / G;
   const int64_t need = (a.ring_units + groups - 1) / groups;
