@@ -42,6 +42,7 @@ import workloads  # noqa: E402
 METRIC = "Gelem/s per optimizer step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "Gelem/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20            # GB300 L2 (about 126 MiB)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -77,6 +78,17 @@ class Workload:
 
     def nstates(self):
         return {"adam": 2, "adamw": 2, "ademamix": 3}.get(self.optim, 1)
+
+    def read_bytes(self):
+        """Bytes a step reads (p, g, states, absmax): what must exceed the L2
+        for back-to-back steps to find none of their inputs there."""
+        e = 4 if self.dtype == "f32" else 2
+        ns, B = self.nstates(), self.blocksize
+        total = 0
+        for n, b in zip(self.sizes, self.bits):
+            nb = 1 if B == 0 else (n + B - 1) // B
+            total += 2 * n * e + (n * ns + nb * 4 * ns if b == 8 else n * 4 * ns)
+        return total
 
     def algorithmic_bytes(self, live_block_frac=1.0):
         e = 4 if self.dtype == "f32" else 2
@@ -457,6 +469,14 @@ def run_gpu(args, wl):
     step_no = [0]
     state_arrays = [t for ps in params for t in (ps.s1, ps.s2, ps.absmax1, ps.absmax2)
                     if t is not None]
+    # Between timed steps: flush the L2, or (inputs well over the L2's size)
+    # run the steps back to back: each then starts with the lines the last
+    # one left, dirty ones included, and none of its own inputs
+    l2_mode = args.l2
+    if l2_mode == "auto":
+        l2_mode = "none" if wl.read_bytes() >= 1.2 * L2_BYTES and not wl.paged else "flush"
+    if l2_mode == "none" and wl.read_bytes() < 1.2 * L2_BYTES:
+        l2_mode = "flush"
 
     def page_out():
         # device-memory pressure elsewhere has moved the states to the host
@@ -504,7 +524,8 @@ def run_gpu(args, wl):
             # so no event pair ever waits for a launch
             gpu_sleep(stream, HOST_AHEAD_STEPS * HOST_AHEAD_US_PER_STEP)
         page_out()
-        flush_l2()
+        if l2_mode == "flush":
+            flush_l2()
         starts[k].record(stream)
         one_step(args.warmup + k)
         ends[k].record(stream)
@@ -549,8 +570,12 @@ def run_gpu(args, wl):
                    "state": "uint8 codes + binary32 absmax",
                    "timing": "median of per-step CUDA event pairs on the launching stream; "
                              "the host enqueues ahead of the device",
-                   "l2": "flushed before every timed step (256 MiB written, then 256 MiB of "
-                         "other data read, leaving clean unrelated lines)",
+                   "l2": ("flushed before every timed step (256 MiB written, then 256 MiB of "
+                          "other data read, leaving clean unrelated lines)" if l2_mode == "flush"
+                          else f"not flushed: the step reads {wl.read_bytes() / 2**20:.0f} MiB, "
+                               f"more than the {L2_BYTES / 2**20:.0f} MiB L2; steps run back to "
+                               "back, each starting with the previous one's lines (dirty ones "
+                               "included)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
@@ -1073,6 +1098,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", default="flush", choices=["flush", "none", "auto"],
+                    help="between timed steps: flush the L2, or run back to back when the "
+                         "step's inputs exceed the L2 (none, auto: back to back where allowed)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the cpu_baseline leg")
     ap.add_argument("--ref-budget", type=float, default=90.0,
