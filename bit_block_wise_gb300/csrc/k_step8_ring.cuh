@@ -830,16 +830,23 @@ __global__ void __launch_bounds__(ring_warps<OPT, SH>() * 32, 1)
             }
           } else {  // LION
             const float2 cc = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
-            float2 u;
-            u.x = cc.x > 0.0f ? 1.0f : (cc.x < 0.0f ? -1.0f : 0.0f);
-            u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
             const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
             sv[0][e] = m.x; sv[0][e + 1] = m.y;
-            if (NORM || BCLIP) add_u2(e, u);
-            if (BCLIP) {
-              ud[e] = u.x; ud[e + 1] = u.y;
-            } else if (!NORM) {
-              pair_apply<OPT>(a, -eff, pp, u);
+            if (NORM || BCLIP) {
+              float2 u;
+              u.x = cc.x > 0.0f ? 1.0f : (cc.x < 0.0f ? -1.0f : 0.0f);
+              u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
+              add_u2(e, u);
+              if (BCLIP) {
+                ud[e] = u.x; ud[e + 1] = u.y;
+              }
+            } else {
+              // p + (-eff)*sign(c) with the product formed by bits: -eff
+              // with c's sign folded in where |c| > 0, else the signed zero
+              // -eff * (+0); the one rounding is the sum's, as in the FMA
+              const float2 t = lion_term(-eff, cc);
+              if (Traits<OPT>::DECOUPLED && a.wd != 0.0f) pp = mul2(pp, f2(a.decay));
+              pp = __fadd2_rn(pp, t);
               p[e] = pp.x; p[e + 1] = pp.y;
             }
           }
