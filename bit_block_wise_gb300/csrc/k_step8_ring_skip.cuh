@@ -345,12 +345,11 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
           p[e] = keep(k0, p[e], pp.x); p[e + 1] = keep(k1, p[e + 1], pp.y);
         } else {  // LION
           const float2 cc = fma2(f2(a.b1), stt[0], mul2(f2(a.omb1), gg));
-          float2 u;
-          u.x = cc.x > 0.0f ? 1.0f : (cc.x < 0.0f ? -1.0f : 0.0f);
-          u.y = cc.y > 0.0f ? 1.0f : (cc.y < 0.0f ? -1.0f : 0.0f);
           const float2 m = fma2(f2(a.b2), stt[0], mul2(f2(a.omb2), gg));
           sv[0][e] = keep(k0, stt[0].x, m.x); sv[0][e + 1] = keep(k1, stt[0].y, m.y);
-          pair_apply<OPT>(a, -eff, pp, u);
+          // p + (-eff)*sign(c), the product formed by bits (lion_term)
+          if (Traits<OPT>::DECOUPLED && a.wd != 0.0f) pp = mul2(pp, f2(a.decay));
+          pp = __fadd2_rn(pp, lion_term(-eff, cc));
           p[e] = keep(k0, p[e], pp.x); p[e + 1] = keep(k1, p[e + 1], pp.y);
         }
       }
