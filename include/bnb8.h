@@ -225,6 +225,9 @@ int bnb8_qmap_code(const float* qmap, float x, uint8_t* code);
  * absmax[b] = max |x| over the block and codes[i] = the number of map
  * midpoints (q[j] + q[j+1]) / 2 strictly below x[i] * (1 / absmax[b])
  * (nearest level, ties to the lower one; 0 / absmax 0 for an all-zero block).
+ * A NaN in a block makes its absmax NaN (the IEEE 754-2019 maximum); the
+ * block is then normalised by 0 as an all-zero block is, so its values take
+ * the code of 0 and the NaN code 0.
  *   x       n elements of dtype.
  *   qmap    256 binary32 map values, strictly ascending (device).
  *   codes   n uint8 (device, written).   absmax  ceil(n/B) binary32 (written).
@@ -257,7 +260,8 @@ size_t bnb8_workspace_size(const bnb8_tensor* tensors, int ntensors, const bnb8_
  *   decoupled decay and wd != 0: p = p * (1 - lr*wd)
  *   p = -(step * clip)*u + p
  * 8-bit states are dequantized (qmap[code] * absmax), updated, and
- * requantized with a fresh per-block absmax after p is written from the
+ * requantized with a fresh per-block absmax (NaN when a new state of the
+ * block is NaN, as in bnb8_quantize_blockwise) after p is written from the
  * unquantized new states.  skip_zeros and max_unorm as in bnb8_hparams.
  *   qmap1, qmap2  device maps (256 binary32, ascending) for s1 and s2 of
  *                 8-bit tensors; unused for 32-bit tensors.

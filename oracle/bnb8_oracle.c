@@ -224,9 +224,26 @@ int oracle_code(const float* mid, float xn) {
 
 /* READING (normalisation): absmax = max |x| over the block (exact); the
  * reciprocal 1/absmax is taken once per block in binary32 (0 for an all-zero
- * block) and each element is normalised by one multiplication. */
+ * block) and each element is normalised by one multiplication.
+ * READING (a NaN in the block): the maximum is the IEEE 754-2019 maximum,
+ * which is NaN when any operand is NaN.  The reciprocal of a NaN absmax is 0
+ * (as for an all-zero block), so every value of the block takes the code of
+ * 0 and the NaN the code of NaN (no midpoint lies below it: code 0); the NaN
+ * absmax makes the whole block NaN when it is next dequantized.  A maximum
+ * that skipped the NaN would instead store it as the lowest level times a
+ * finite absmax: a finite, wrong state. */
 static float block_inverse(float absmax) {
   return absmax > 0.0f ? 1.0f / absmax : 0.0f;
+}
+/* max |x| over x[0..n) with the IEEE 754-2019 maximum's NaN rule */
+static float block_absmax(const float* x, int64_t n) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (isnan(a)) return a;
+    if (a > amax) amax = a;
+  }
+  return amax;
 }
 
 /* [P4] abstract: block-wise quantization splits the tensor into blocks of B
@@ -240,9 +257,10 @@ void oracle_quantize_blockwise(const void* x, int dtype, int64_t n, const float*
   int64_t nblocks = (n + B - 1) / B;
   for (int64_t b = 0; b < nblocks; ++b) {
     int64_t lo = b * B, hi = lo + B < n ? lo + B : n;
-    float amax = 0.0f;
+    float amax = 0.0f;   /* as block_absmax, over the block's loaded values */
     for (int64_t i = lo; i < hi; ++i) {
       float a = fabsf(load_elem(x, dtype, i));
+      if (isnan(a)) { amax = a; break; }
       if (a > amax) amax = a;
     }
     absmax[b] = amax;
@@ -621,11 +639,7 @@ float oracle_step_clipped(const oracle_hparams* hp, void* p, const void* g, void
     for (int64_t i = lo; i < hi; ++i)
       if (!skipped[i - lo]) store_elem(p, dtype, i, pnew[i - lo]);
     for (int j = 0; j < ns; ++j) {
-      float amax = 0.0f;
-      for (int64_t i = lo; i < hi; ++i) {
-        float a = fabsf(snew[j * B + (i - lo)]);
-        if (a > amax) amax = a;
-      }
+      float amax = block_absmax(snew + j * B, hi - lo);
       st[j].absmax[b] = amax;
       float inv = block_inverse(amax);
       uint8_t* codes = (uint8_t*)st[j].base;

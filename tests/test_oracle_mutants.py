@@ -82,9 +82,12 @@ MUTANTS = [
      [(pins.test_skip_zeros_identities, ("adam", 8, "f32"))]),
     ("fully skipped block requantized", "if (!any_update) continue;", "if (0) continue;",
      [(pins.test_skip_zeros_identities, ("momentum", 8, "f32"))]),
-    ("requantization absmax without |.|", "float a = fabsf(snew[j * B + (i - lo)]);",
-     "float a = snew[j * B + (i - lo)];",
+    ("requantization absmax without |.|", "float a = fabsf(x[i]);", "float a = x[i];",
      [(pins.test_8bit_step_tracks_32bit, ("momentum", "f32"))]),
+    ("requantization absmax skips a NaN", "    if (isnan(a)) return a;\n", "",
+     [(pins.test_step_nan_state_makes_its_block_absmax_nan, ())]),
+    ("quantization absmax skips a NaN", "      if (isnan(a)) { amax = a; break; }\n", "",
+     [(pins.test_quantize_nan_makes_its_block_absmax_nan, ())]),
     ("AdEMAMix m2 aliases m1", "out[1].base = (char*)s1 + n * esz;", "out[1].base = (char*)s1;",
      [(pins.test_8bit_step_tracks_32bit, ("ademamix", "f32"))]),
     ("update norm not squared",

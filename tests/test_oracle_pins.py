@@ -228,6 +228,47 @@ def test_quantize_zero_block_is_zero_code():
         assert q[zc] == 0.0
 
 
+def test_quantize_nan_makes_its_block_absmax_nan():
+    """READING (a NaN in the block): absmax is the IEEE 754-2019 maximum, NaN
+    when any |x| is; the block is then normalised by 0 like an all-zero
+    block (every value takes the code of 0, the NaN code 0), and the other
+    blocks are as if quantized alone."""
+    x = workloads.normal(600, 0.1, 3).astype(np.float32)
+    x[10] = np.nan
+    for q, zc in ((S, 127), (U, 0)):
+        codes, absmax = oracle.quantize_blockwise(x, "f32", q, 256)
+        assert np.isnan(absmax[0]) and not np.isnan(absmax[1:]).any()
+        assert codes[10] == 0
+        assert np.all(np.delete(codes[:256], 10) == zc)
+        c2, a2 = oracle.quantize_blockwise(x[256:], "f32", q, 256)
+        assert np.array_equal(codes[256:], c2) and np.array_equal(absmax[1:], a2)
+
+
+def test_step_nan_state_makes_its_block_absmax_nan():
+    """The same reading in the step: a NaN gradient gives a NaN first moment,
+    so that block's absmax is NaN and its codes are the code of 0 (the NaN's:
+    0); p takes the NaN, every other element and block steps as without it."""
+    n, B = 700, 256
+    g = workloads.normal(n, 1e-2, 11).astype(np.float32)
+    ohp = oracle.HParams(optim="momentum", lr=0.01, beta1=0.9, step=1)
+    runs = []
+    for bad in (True, False):
+        gg = g.copy()
+        if bad:
+            gg[300] = np.nan
+        p = workloads.normal(n, 0.1, 12).astype(np.float32)
+        t = oracle.TensorState(p, *oracle.zero_state("momentum", n, 8, B, S, None), 8)
+        oracle.step(ohp, t, gg, "f32", B, S, None)
+        runs.append(t)
+    nan_run, ref = runs
+    assert np.isnan(nan_run.absmax1[1]) and np.isnan(nan_run.p[300])
+    assert nan_run.s1[300] == 0 and np.all(np.delete(nan_run.s1[256:512], 300 - 256) == 127)
+    keep = np.r_[0:256, 512:n]
+    assert np.array_equal(nan_run.s1[keep], ref.s1[keep])
+    assert np.array_equal(nan_run.absmax1[[0, 2]], ref.absmax1[[0, 2]])
+    assert np.array_equal(np.delete(nan_run.p, 300), np.delete(ref.p, 300))
+
+
 def test_quantize_half_inputs_widen_exactly():
     rng = np.random.default_rng(5)
     x = rng.standard_normal(1000).astype(np.float32)
