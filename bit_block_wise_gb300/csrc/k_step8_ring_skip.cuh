@@ -60,6 +60,80 @@ struct SkipSmem {
   static constexpr int kBytes = kLiveBars + kWarps * 8;
 };
 
+// A lane's 8 gradient elements of one pass as they sit in a stage (the
+// layout of stage_load: one 16-byte word group for 16-bit values, two for
+// binary32), before they are widened.
+template <int DT>
+struct RawG {
+  uint4 w[DT == DT_F32 ? 2 : 1];
+};
+template <int DT>
+__device__ __forceinline__ void stage_raw(const unsigned char* base, int lane, int q0, RawG<DT>& r) {
+  if (DT == DT_F32) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) r.w[i] = reinterpret_cast<const uint4*>(base + (q0 + i) * 512)[lane];
+  } else {
+    r.w[0] = reinterpret_cast<const uint4*>(base + (q0 / 2) * 512)[lane];
+  }
+}
+// The same from global memory (a ragged chunk), absent elements as 0.
+template <int DT>
+__device__ __forceinline__ void global_raw(const void* base, int64_t e0, int v, int lane, int q0,
+                                           RawG<DT>& r) {
+  if (DT == DT_F32) {
+    const uint32_t* b = static_cast<const uint32_t*>(base) + e0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int o = quad_offset<DT>(lane, q0 + i);
+      r.w[i].x = o < v ? b[o] : 0u;
+      r.w[i].y = o + 1 < v ? b[o + 1] : 0u;
+      r.w[i].z = o + 2 < v ? b[o + 2] : 0u;
+      r.w[i].w = o + 3 < v ? b[o + 3] : 0u;
+    }
+  } else {
+    const uint16_t* b = static_cast<const uint16_t*>(base) + e0;
+    const int o = quad_offset<DT>(lane, q0);   // 8 consecutive elements
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = o + k < v ? b[o + k] : 0u;
+    r.w[0] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                        h[6] | (h[7] << 16));
+  }
+}
+template <int DT>
+__device__ __forceinline__ void raw_zero(RawG<DT>& r) {
+#pragma unroll
+  for (int i = 0; i < (DT == DT_F32 ? 2 : 1); ++i) r.w[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+// Whether any of the 8 values is nonzero: the OR of their magnitude bits
+// (+0 and -0 are zero; subnormals, infinities and NaN are not), which is
+// the comparison g != 0 on each value.
+template <int DT>
+__device__ __forceinline__ bool raw_nonzero(const RawG<DT>& r) {
+  constexpr uint32_t kMag = DT == DT_F32 ? 0x7fffffffu : 0x7fff7fffu;
+  uint32_t o = 0u;
+#pragma unroll
+  for (int i = 0; i < (DT == DT_F32 ? 2 : 1); ++i) o |= r.w[i].x | r.w[i].y | r.w[i].z | r.w[i].w;
+  return (o & kMag) != 0u;
+}
+// The values, in stage_load's order.
+template <int DT>
+__device__ __forceinline__ void raw_widen(const RawG<DT>& r, float (&x)[8]) {
+  if (DT == DT_F32) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      x[4 * i] = __uint_as_float(r.w[i].x); x[4 * i + 1] = __uint_as_float(r.w[i].y);
+      x[4 * i + 2] = __uint_as_float(r.w[i].z); x[4 * i + 3] = __uint_as_float(r.w[i].w);
+    }
+  } else {
+    const uint4 v = r.w[0];
+    x[0] = lo_half(v.x, DT); x[1] = hi_half(v.x, DT);
+    x[2] = lo_half(v.y, DT); x[3] = hi_half(v.y, DT);
+    x[4] = lo_half(v.z, DT); x[5] = hi_half(v.z, DT);
+    x[6] = lo_half(v.w, DT); x[7] = hi_half(v.w, DT);
+  }
+}
+
 // WHOLE: every tensor of the launch is aligned for bulk copies and a
 // multiple of 512 elements (the host checked it).
 template <int OPT, int DT, bool WHOLE>
@@ -188,21 +262,18 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
     const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
     const bool vec = WHOLE || (d.vec_ok & 1) != 0;
 
-    // ---- the gradient of both blocks of the chunk ----
-    float gc[2][8];
+    // ---- the gradient of both blocks of the chunk: from a stage as raw
+    // ---- words (whether a block is live is a test on their bits; only a
+    // ---- live block's are widened), from global memory as values ----
+    RawG<DT> gr[2];
     int vbs[2];
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       const int rest = c.v - 256 * pass;
       vbs[pass] = WHOLE ? 256 : (rest > 256 ? 256 : (rest > 0 ? rest : 0));
-      if (staged) {
-        stage_load<DT, 2>(ring + s * L::kStage + L::kSG, lane, 2 * pass, gc[pass]);
-      } else if (!WHOLE && have && vbs[pass] > 0) {
-        global_load<DT, 2>(d.g, c.e0, c.v, lane, 2 * pass, gc[pass]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gc[pass][e] = 0.0f;
-      }
+      if (staged) stage_raw<DT>(ring + s * L::kStage + L::kSG, lane, 2 * pass, gr[pass]);
+      else if (!WHOLE && have && vbs[pass] > 0) global_raw<DT>(d.g, c.e0, c.v, lane, 2 * pass, gr[pass]);
+      else raw_zero<DT>(gr[pass]);   // (absent elements read as 0)
     }
     // refill this stage with the warp's next chunk
     __syncwarp();
@@ -226,13 +297,11 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
     // a block whose raw gradient is all zero is left as it is
     bool blk_live[2];
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      bool nz = false;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) nz = nz || gc[pass][e] != 0.0f;   // (absent elements read as 0)
-      blk_live[pass] = __any_sync(0xffffffffu, nz);
-    }
+    for (int pass = 0; pass < 2; ++pass) blk_live[pass] = __any_sync(0xffffffffu, raw_nonzero<DT>(gr[pass]));
     if (!blk_live[0] && !blk_live[1]) continue;
+    float gc[2][8];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) raw_widen<DT>(gr[pass], gc[pass]);
 
     // ---- the live chunk's p, codes and absmax, one round trip ----
     const bool bulk = WHOLE || (c.v == kChunk && (d.vec_ok & 2));
