@@ -172,8 +172,10 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
     int32_t k = 0;
     if (lane == 0) k = atomicAdd(&s_next, 1);
     k = __shfl_sync(0xffffffffu, k, 0);
-    const int64_t u = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
-    return u < TB ? static_cast<int32_t>(u) : TB;
+    // (k exceeds TB / gridDim by at most one take per stage of each warp,
+    // so u does not wrap)
+    const uint32_t u = blockIdx.x + static_cast<uint32_t>(k) * gridDim.x;
+    return u < static_cast<uint32_t>(TB) ? static_cast<int32_t>(u) : TB;
   };
 
   // ---- the ring of gradient chunks, and the live buffer ----
@@ -259,9 +261,6 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
         staged = true;
       }
     }
-    const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
-    const bool vec = WHOLE || (d.vec_ok & 1) != 0;
-
     // ---- the gradient of both blocks of the chunk: from a stage as raw
     // ---- words (whether a block is live is a test on their bits; only a
     // ---- live block's are widened), from global memory as values ----
@@ -302,6 +301,8 @@ __global__ void __launch_bounds__(24 * 32, 1) k_step8_skip_ring(const __grid_con
     float gc[2][8];
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) raw_widen<DT>(gr[pass], gc[pass]);
+    const float eff = a.step_size * (a.clip != nullptr ? a.clip[d.index] : 1.0f);
+    const bool vec = WHOLE || (d.vec_ok & 1) != 0;
 
     // ---- the live chunk's p, codes and absmax, one round trip ----
     const bool bulk = WHOLE || (c.v == kChunk && (d.vec_ok & 2));
