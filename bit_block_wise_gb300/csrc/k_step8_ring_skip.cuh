@@ -15,7 +15,10 @@
 // round trip per chunk), and its live blocks are stepped and requantized
 // exactly as in the plain step, with the skipped elements' old parameter and
 // dequantized states kept.  Blocks with an all-zero gradient cost a
-// shared-memory read and a warp vote.
+// shared-memory read and a warp vote on the OR of the raw gradient words'
+// magnitude bits; only live blocks are widened to binary32.  The warps of a
+// CTA take their chunks from a shared counter, so that the warp that meets
+// more live chunks takes fewer.
 #pragma once
 
 #include "k_step8_ring.cuh"
