@@ -539,6 +539,21 @@ def test_step_max_unorm_per_block_blocksizes(bnb8, qdev, B, dtype):
              seed=61, extra_hp=dict(unorm_per_block=True))
 
 
+@pytest.mark.parametrize("optim", ["adam", "lion", "rmsprop", "ademamix"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_skip_zeros_tensor_lists(bnb8, qdev, optim, dtype):
+    """skip_zeros at B = 256 (the gradient-only ring) over a long list:
+    whole-chunk and ragged tensors (launched apart), misaligned storage (the
+    copies replaced by plain loads), and more tensors than one launch takes,
+    so that the chunks a warp takes from its CTA's counter jump across
+    tensors."""
+    rng = np.random.default_rng(81)
+    sizes = [int(x) for x in rng.integers(1, 2600, size=110)] + [512 * 7, 256 * 9 + 100, 1024 * 3]
+    offsets = [1 if i % 17 == 5 else 0 for i in range(len(sizes))]
+    run_case(bnb8, qdev, optim, dtype, 8, 256, sizes, steps=2, skip_zeros=True, zero_frac=0.4,
+             wd=1e-2, seed=83, offsets=offsets)
+
+
 @pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
 def test_step_max_unorm_per_block_skip_zeros(bnb8, qdev, optim):
     run_case(bnb8, qdev, optim, "bf16", [8, 32], 256, [6 * 256 + 3, 700], steps=3,
