@@ -83,6 +83,22 @@ def test_algorithmic_bytes_model():
         bench.WORKLOADS["gpt2xl_carried"]().algorithmic_bytes()
 
 
+def test_read_bytes_and_the_pages_baseline():
+    # what a step reads (p, g, codes, absmax), against the L2 for --l2 none
+    wl = bench.WORKLOADS["adam_4096"]()
+    n = 4096 * 4096
+    assert wl.read_bytes() == 2 * 4 * n + 2 * n + 2 * 4 * (n // 256)
+    assert wl.read_bytes() >= 1.2 * bench.L2_BYTES
+    assert bench.WORKLOADS["adam_small"]().read_bytes() < 1.2 * bench.L2_BYTES
+    # vs_baseline only where the pages give a figure for the workload: the
+    # PR #1692 step, 1.2875 ms for 4096 x 4096 elements
+    pages = bench.WORKLOADS["adam_4096_bf16_pages"]()
+    gelem = n / 1.2875e-3 / 1e9
+    assert bench.vs_pages(pages, 10 * gelem) == 10.0
+    assert bench.vs_pages(wl, 100.0) is None
+    assert bench.WORKLOADS["ademamix_4096_bf16_pages"]().pages == pages.pages
+
+
 def test_clock_summary():
     rows = [dict(t=1.0, sm=1900.0, sm_max=2070.0, power="900", hw="Not Active",
                  hw_thermal="Not Active", sw_thermal="Not Active", sw_power="Active"),
