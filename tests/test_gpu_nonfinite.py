@@ -114,7 +114,7 @@ def _run(bnb8, optim, dtype, bits, B, n, steps=2, skip_zeros=False, init="random
 
 
 @pytest.mark.parametrize("optim", ["adam", "momentum", "rmsprop", "lion", "ademamix"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("B", [256, 2048])
 def test_nonfinite_gradients_on_the_ring(bnb8, optim, dtype, B):
     _run(bnb8, optim, dtype, 8, B, 5 * B + 77)

@@ -554,6 +554,17 @@ def test_skip_zeros_tensor_lists(bnb8, qdev, optim, dtype):
              wd=1e-2, seed=83, offsets=offsets)
 
 
+@pytest.mark.parametrize("optim", ["adam", "lion", "rmsprop", "ademamix"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_step_max_unorm_per_tensor_skip_zeros(bnb8, qdev, optim, dtype):
+    """Per-tensor max_unorm with skip_zeros: the pre-pass over a gradient
+    with zero elements and all-zero blocks, the reduction, then the
+    skip_zeros step (at B = 256 the gradient-only ring) applying each
+    tensor's multiplier to its live blocks."""
+    run_case(bnb8, qdev, optim, dtype, [8, 32, 8], 256, [6 * 512 + 100, 300, 256 * 9], steps=3,
+             skip_zeros=True, zero_frac=0.3, wd=1e-2, max_unorm=0.05, seed=64)
+
+
 @pytest.mark.parametrize("optim", ["adam", "momentum", "ademamix"])
 def test_step_max_unorm_per_block_skip_zeros(bnb8, qdev, optim):
     run_case(bnb8, qdev, optim, "bf16", [8, 32], 256, [6 * 256 + 3, 700], steps=3,
