@@ -908,32 +908,35 @@ __global__ void __launch_bounds__(ring_warps<OPT, SH>() * 32, 1)
                           mul2(f2(a.alpha_t), make_float2(sv[1][e], sv[1][e + 1])));
             return make_float2(sv[0][e], sv[0][e + 1]);
           };
-          if (fast) {
-#pragma unroll
-            for (int e = 0; e < NE; e += 2) {
-              const float2 u = ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              if (NORM || BCLIP) add_u2(e, u);
-              if (BCLIP) {
-                ud[e] = u.x; ud[e + 1] = u.y;
-              } else if (!NORM) {
-                float2 pp = make_float2(p[e], p[e + 1]);
-                pair_apply<OPT>(a, -eff, pp, u);
-                p[e] = pp.x; p[e + 1] = pp.y;
-              }
+          // the direction of elements e, e + 1 into the sums, the kept
+          // directions or the new p
+          auto use_u = [&](int e, float2 u) {
+            if (NORM || BCLIP) add_u2(e, u);
+            if (BCLIP) {
+              ud[e] = u.x; ud[e + 1] = u.y;
+            } else if (!NORM) {
+              float2 pp = make_float2(p[e], p[e + 1]);
+              pair_apply<OPT>(a, -eff, pp, u);
+              p[e] = pp.x; p[e + 1] = pp.y;
             }
+          };
+          // RMSprop, Adagrad: a lane whose numerators (the scaled gradients)
+          // are all +-0 has u = n exactly, since then d = sqrt(v) + eps > 0
+          // (no v is NaN, eps > 0) and +-0 / d = +-0: the untouched rows of
+          // an embedding skip the square root and the division
+          const bool zero_n = (OPT == RMSPROP || OPT == ADAGRAD) && nmax == 0u &&
+                              vmax <= 0x7f800000u && a.eps_hat > 0.0f;
+          if (zero_n) {
+#pragma unroll
+            for (int e = 0; e < NE; e += 2) use_u(e, numer(e));
+          } else if (fast) {
+#pragma unroll
+            for (int e = 0; e < NE; e += 2)
+              use_u(e, ratio2_fast(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
           } else {
 #pragma unroll
-            for (int e = 0; e < NE; e += 2) {
-              const float2 u = ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat);
-              if (NORM || BCLIP) add_u2(e, u);
-              if (BCLIP) {
-                ud[e] = u.x; ud[e + 1] = u.y;
-              } else if (!NORM) {
-                float2 pp = make_float2(p[e], p[e + 1]);
-                pair_apply<OPT>(a, -eff, pp, u);
-                p[e] = pp.x; p[e + 1] = pp.y;
-              }
-            }
+            for (int e = 0; e < NE; e += 2)
+              use_u(e, ratio2_ieee_slow(numer(e), make_float2(sv[kV][e], sv[kV][e + 1]), a.eps_hat));
           }
         }
         if (NORM || BCLIP) {
